@@ -1,1 +1,14 @@
-"""GB300-native fused attention forward."""
+"""GB300-native (sm_103a) fused scaled-dot-product attention forward.
+
+``fwd(q, k, v, scale, causal) -> (o, lse)`` runs the hand-written tcgen05 /
+TMA kernel of ``csrc/attn_fwd.cu`` through its C ABI (``include/attn.h``).
+``build()`` compiles that library in place with nvcc.
+"""
+from ._binding import (ATTN_ECUDA, ATTN_EINVAL, ATTN_ETIMEOUT, ATTN_EUNSUPPORTED, ATTN_OK,
+                       EXPORTS, AttnError, attn_fwd, debug_set, fwd, get_status, load_library,
+                       strerror, version)
+from ._build import LIB_PATH, build
+
+__all__ = ["fwd", "attn_fwd", "get_status", "debug_set", "strerror", "version", "build",
+           "load_library", "LIB_PATH", "EXPORTS", "AttnError", "ATTN_OK", "ATTN_EINVAL",
+           "ATTN_EUNSUPPORTED", "ATTN_ECUDA", "ATTN_ETIMEOUT"]

@@ -1,0 +1,119 @@
+"""ctypes binding of ``libattn.so`` -- argument marshalling only.
+
+Every step of the forward runs in the library's CUDA kernel; PyTorch is used
+here only to allocate device memory and to name the current stream.  There
+is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from ._build import LIB_PATH
+
+ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = 0, 1, 2, 3, 4
+
+# Every symbol the C header declares; the CPU tests check they are exported.
+EXPORTS = ("attn_fwd", "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} (code {code})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: build it with "
+                    "attention_forward_12_gb300.build() (nvcc, sm_103a)")
+            lib = ctypes.CDLL(path)
+            vp, i32 = ctypes.c_void_p, ctypes.c_int
+            lib.attn_fwd.restype = i32
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                     ctypes.c_float, i32, vp]
+            lib.attn_strerror.restype = ctypes.c_char_p
+            lib.attn_strerror.argtypes = [i32]
+            lib.attn_get_status.restype = i32
+            lib.attn_get_status.argtypes = [vp]
+            lib.attn_debug_set.restype = i32
+            lib.attn_debug_set.argtypes = [ctypes.c_ulonglong, i32]
+            lib.attn_version.restype = i32
+            lib.attn_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load_library().attn_strerror(int(code)).decode()
+
+
+def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None,
+             B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+             stream: int | None) -> int:
+    """Direct call of the C entry point with raw device pointers; returns the code."""
+    return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
+                                   int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
+                                   stream)
+
+
+def _current_stream_ptr(device) -> int:
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse=None,
+        want_lse: bool = True):
+    """O = softmax(scale * Q K^T) V on the GPU; returns (o, lse).
+
+    q: fp16 CUDA tensor [B,H,Nq,D], k and v: [B,H,Nk,D], contiguous.
+    scale defaults to 1/sqrt(D).  out / lse may be preallocated
+    ([B,H,Nq,D] fp16 and [B,H,Nq] fp32).  Runs on the current stream.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float16):
+            raise TypeError(f"{name} must be a CUDA float16 tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D [B,H,N,D] tensor")
+    B, H, Nq, D = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError("k and v must be [B,H,Nk,D] with q's B, H and D")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    code = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, D, scale, causal,
+                    _current_stream_ptr(q.device))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd")
+    return out, lse
+
+
+def get_status(stream: int | None = None) -> int:
+    """Synchronise the stream and read-and-clear the device status word."""
+    if stream is None:
+        stream = _current_stream_ptr(None)
+    return load_library().attn_get_status(stream)
+
+
+def debug_set(wait_timeout_ns: int = 2_000_000_000, drop_kv_tile: int = -1) -> int:
+    return load_library().attn_debug_set(int(wait_timeout_ns), int(drop_kv_tile))
+
+
+def version() -> int:
+    return load_library().attn_version()

@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 attention forward: one JSON line on rank 0.
+
+A step is one attention forward over the whole workload (every row of every
+head), inputs already resident in HBM.  The default workload is the long,
+non-causal, D=128 shape [B=4, H=32, N=16384, D=128] with Q, K ~ N(0, 3^2);
+``--workload`` picks another of ``synth.WORKLOADS``.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the same workload on
+its own GPU; (b, h) problems are independent, so there is no data-path
+collective and the scaling is weak.  Timing takes the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_forward_12_gb300 import synth  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and µs/call at 1 GB300; % of dense FP16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "peaked_4x32x16384x128"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAK_TFLOPS = 1900.0  # dense bf16 burst, used only without a measured-peaks file
+
+
+def flops(w: synth.Workload) -> float:
+    """4*B*H*Nq*Nk*D, halved when causal (two matmuls of 2*N*N*D each)."""
+    f = 4.0 * w.B * w.H * w.Nq * w.Nk * w.D
+    return f / 2 if w.causal else f
+
+
+def algorithmic_bytes(w: synth.Workload) -> int:
+    """Q, K, V read once, O and LSE written once."""
+    return 2 * w.B * w.H * (w.Nq * w.D * 2 + w.Nk * w.D * 2) + 4 * w.B * w.H * w.Nq
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return None, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in ("attention_forward_12_gb300/csrc/attn_fwd.cu",
+                "attention_forward_12_gb300/csrc/sm103_primitives.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_digest") != kernel_source_digest():
+        return None, None
+    return ent.get("dram_bytes_per_launch"), ent.get("note")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                clk, cmax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, q, k, v, seconds: float, seed: int):
+    """Time the fp64 oracle on a bounded row sample (~`seconds` of CPU work).
+
+    Returns (rows, O, LSE, elapsed, threads, flops_done).
+    """
+    import numpy as np
+    import oracle
+    gen = np.random.Generator(np.random.Philox(key=[seed, 1234]))
+    calib = np.sort(gen.choice(w.B * w.H * w.Nq, size=min(64, w.B * w.H * w.Nq), replace=False))
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.scale, w.causal, calib)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(w.B * w.H * w.Nq, max(64, len(calib) * seconds / dt)))
+    rows = np.sort(gen.choice(w.B * w.H * w.Nq, size=n, replace=False))
+    t0 = time.perf_counter()
+    O, L, threads = oracle.attn_rows(q, k, v, w.scale, w.causal, rows)
+    el = time.perf_counter() - t0
+    done = 0.0
+    for r in rows:  # exact flops of the sampled rows (causal rows differ)
+        i = int(r) % w.Nq
+        done += 4.0 * (min(i + 1, w.Nk) if w.causal else w.Nk) * w.D
+    return rows, O, L, el, threads, done
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 CPU oracle as it stands, on host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    q, k, v = synth.workload_qkv(w)
+    total = args.steps + args.warmup
+    per_step = max(0.2, min(10.0, 150.0 / max(total, 1)))
+    times, rates = [], []
+    threads = 0
+    nrows = 0
+    for s in range(total):
+        rows, _, _, el, threads, done = oracle_sample(w, q, k, v, per_step, seed=w.seed + s)
+        if s >= args.warmup:
+            times.append(el)
+            rates.append(done / el / 1e12)
+            nrows = len(rows)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{nrows} random query rows of the workload per step "
+                                   f"(~{per_step:.1f} s of CPU work each)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
+            "causal": w.causal, "scale": w.scale, "sigma_qk": w.sigma_qk, "sigma_v": w.sigma_v,
+            "seed": w.seed,
+            "l2": ("inputs larger than L2 (%.0f MB > 129 MB); no flush" % (algorithmic_bytes(w) / 1e6))
+            if algorithmic_bytes(w) > L2_BYTES else "L2 flushed between steps (256 MB write)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,D,causal: a custom N(0,1) workload instead of --workload "
+                         "(used for small profiling captures)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.shape:
+        B, H, N, D, c = (int(x) for x in args.shape.split(","))
+        w = synth.Workload(f"custom_{B}x{H}x{N}x{D}{'_causal' if c else ''}", B, H, N, N, D,
+                           bool(c), 1.0, 1.0, 42)
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import attention_forward_12_gb300 as attn
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    attn.load_library()
+
+    # inputs: seeded on the host (the same bytes the oracle sees), copied once
+    qn, kn, vn = synth.workload_qkv(w)
+    q = torch.from_numpy(qn).to(dev)
+    k = torch.from_numpy(kn).to(dev)
+    v = torch.from_numpy(vn).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    flush = None
+    if algorithmic_bytes(w) <= L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        if flush is not None:
+            flush.fill_(1)
+        code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
+        if code != attn.ATTN_OK:
+            raise attn.AttnError(code, "attn_fwd")
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if attn.get_status(sptr) != attn.ATTN_OK:
+        raise RuntimeError("kernel status error during warm-up")
+
+    # ---------------- device-timed region: K steps, inputs resident
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t_start.record(stream)
+        for s in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            ev[s][0].record(stream)
+            code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
+            ev[s][1].record(stream)
+            if code != attn.ATTN_OK:
+                raise attn.AttnError(code, "attn_fwd")
+        t_end.record(stream)
+        barrier()
+    status = attn.get_status(sptr)
+    if status != attn.ATTN_OK:
+        raise RuntimeError(f"kernel status {status} in the timed region")
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        step_ms = statistics.mean(kernel_ms)
+    else:
+        step_ms = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    f = flops(w)
+    value = world * f / (step_ms * 1e-3) / 1e12
+    kern_avg_ms = statistics.mean(kernel_ms)
+
+    # ---------------- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (qn, kn, vn))
+        ho = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
+            if code != attn.ATTN_OK:
+                raise attn.AttnError(code, "attn_fwd")
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e_ms = a.elapsed_time(b) / n_e2e
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * f / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "steps": n_e2e,
+               "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+               "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4)}
+        assert attn.get_status(sptr) == attn.ATTN_OK
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = read_peaks()
+    if peaks:
+        peak = float(peaks["bf16_tflops"])  # fp16 dense rate = bf16 dense rate (nominal 1:1)
+        peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    else:
+        peak = peak_sus = FALLBACK_PEAK_TFLOPS
+    achieved = f / (kern_avg_ms * 1e-3) / 1e12
+    traffic, traffic_note = recorded_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}; fp16 dense = bf16 dense",
+                "peak_sustained": peak_sus, "frac_sustained": achieved / peak_sus,
+                "frac_of_nominal_2250": achieved / 2250.0,
+                "kernel_ms_avg": kern_avg_ms, "kernel_ms_min": min(kernel_ms),
+                "algorithmic_flops_per_launch": f}
+    if traffic_note:
+        roofline["traffic_note"] = traffic_note
+
+    cpu = None
+    if world == 1:
+        rows, O, L, el, threads, done = oracle_sample(w, qn, kn, vn, args.cpu_seconds, seed=w.seed)
+        import numpy as np
+        og = o.view(-1, w.D)[torch.from_numpy(rows).to(dev)].float().cpu().numpy().astype(np.float64)
+        lg = lse.view(-1)[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
+        cpu = {"value": done / el / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(rows)} random query rows of the same workload (fp64 oracle, "
+                         f"{el:.1f} s)",
+               "gpu_vs_oracle_on_sample": {"o_max_abs": float(np.abs(og - O).max()),
+                                           "o_rel_rms": float(np.linalg.norm(og - O) / np.linalg.norm(O)),
+                                           "lse_max_abs": float(np.abs(lg - L).max())}}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
+        "pct_of_peak": 100.0 * value / world / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": config_of(w), "parallelism": f"replicas x{world} (independent problems)",
+        "gpu_launches": args.steps, "roofline": roofline, "clocks": clk.summary(),
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

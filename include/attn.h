@@ -1,0 +1,97 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * The operation is the one the pages build up in "Learning FlashAttention
+ * the Hard Way -- Part 2" (problem statement: F.scaled_dot_product_attention
+ * on fp16 [B,H,N,D] tensors, the SDPA_P / SDPA_L shapes; the streaming
+ * (m, d, o) reduction of sections "Move 0" and "Move 1 -- Tensor Cores"):
+ *
+ *     O[b,h,i,:] = sum_j softmax_j(scale * q[b,h,i,:] . k[b,h,j,:]) v[b,h,j,:]
+ *     LSE[b,h,i] = log sum_j exp(scale * q[b,h,i,:] . k[b,h,j,:])   (natural log)
+ *
+ * over the admissible keys j: all 0 <= j < Nk, or, when causal, only j <= i
+ * (top-left alignment: key j is masked when j > i, as torch's is_causal).
+ * The N x N scores never reach global memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers to tensors are DEVICE pointers on the current CUDA device.
+ *     The caller owns every buffer; the library allocates nothing per call.
+ *   - Layout is contiguous row-major: q and o are [B,H,Nq,D], k and v are
+ *     [B,H,Nk,D], lse is [B,H,Nq]; element (b,h,n,d) of q is at
+ *     ((b*H + h)*Nq + n)*D + d.
+ *   - q, k, v, o are IEEE binary16 (fp16); lse is fp32.  Products are
+ *     accumulated in fp32; the softmax weights are rounded to fp16 before
+ *     they multiply V (as the page's C->A repack rounds P with cvt.rn).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on that stream; they perform no host synchronisation
+ *     and no allocation.
+ *   - Return values are ATTN_* codes below.  Argument errors are detected on
+ *     the host before anything is enqueued.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_VERSION 1
+
+enum {
+  ATTN_OK = 0,
+  ATTN_EINVAL = 1,        /* null tensor pointer, negative size, Nk < 1, scale < 0 or not finite */
+  ATTN_EUNSUPPORTED = 2,  /* D not in {64,128}, misaligned pointer, overlapping output,
+                             B*H > 65535, or a device other than sm_103 */
+  ATTN_ECUDA = 3,         /* tensor-map encoding or kernel launch failed */
+  ATTN_ETIMEOUT = 4       /* reported by attn_get_status: a kernel wait ran out */
+};
+
+/*
+ * attn_fwd -- O = softmax(scale * Q K^T) V and LSE, fp16 in/out.
+ *
+ *   q      [B,H,Nq,D] fp16, 16-byte aligned.
+ *   k, v   [B,H,Nk,D] fp16, 16-byte aligned.
+ *   o      [B,H,Nq,D] fp16, 16-byte aligned, written; must not overlap q, k, v.
+ *   lse    [B,H,Nq] fp32, 4-byte aligned, written; may be NULL (not computed).
+ *   B, H, Nq >= 0 (any of them 0: nothing is done, ATTN_OK), Nk >= 1,
+ *   B*H <= 65535, D in {64, 128}.
+ *   scale  softmax scale, finite and >= 0 (the pages use 1/sqrt(D)).
+ *   causal 0: every key is admissible; nonzero: key j masked when j > i.
+ *
+ * Errors: ATTN_EINVAL / ATTN_EUNSUPPORTED for bad arguments (nothing is
+ * enqueued), ATTN_ECUDA if encoding the TMA descriptors or the launch fails.
+ * A kernel whose internal wait runs out stops early, leaves o / lse
+ * undefined and records ATTN_ETIMEOUT for attn_get_status().  While that
+ * status word is set, later launches on the device do no work (their
+ * outputs are undefined) until attn_get_status() reads and clears it.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+             int Nk, int D, float scale, int causal, void* stream);
+
+/* Human-readable text for an ATTN_* code.  Never NULL. */
+const char* attn_strerror(int code);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: ATTN_OK, or the first error a kernel recorded since the last call
+ * (ATTN_ETIMEOUT).  Returns ATTN_ECUDA if the synchronisation itself fails.
+ */
+int attn_get_status(void* stream);
+
+/*
+ * Testing hook.  Sets the limit of every kernel wait (nanoseconds of GPU
+ * global time, default 2e9) and, when drop_kv_tile >= 0, makes the producer
+ * skip the K load of that key tile so that the wait for it runs out; -1
+ * restores normal operation.  Affects calls made after it, process-wide.
+ * Returns ATTN_EINVAL for a zero timeout or drop_kv_tile < -1.
+ */
+int attn_debug_set(unsigned long long wait_timeout_ns, int drop_kv_tile);
+
+/* ATTN_VERSION of the library. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

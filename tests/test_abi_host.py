@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads,
+exports every symbol include/attn.h declares, and rejects bad arguments
+before touching the device."""
+import os
+import re
+
+import pytest
+
+import attention_forward_12_gb300 as attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn.build()
+    return attn.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_and_binding_agree(lib):
+    decl = declared_functions()
+    assert decl, "no declarations parsed from include/attn.h"
+    assert sorted(attn.EXPORTS) == decl
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strerror(lib):
+    assert attn.version() == 1
+    for code in (attn.ATTN_OK, attn.ATTN_EINVAL, attn.ATTN_EUNSUPPORTED, attn.ATTN_ECUDA,
+                 attn.ATTN_ETIMEOUT, 99):
+        assert isinstance(attn.strerror(code), str) and attn.strerror(code)
+
+
+A = 1 << 20  # a 16-byte aligned fake address: validation never dereferences it
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, A, A, 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0), attn.ATTN_EINVAL),      # null q
+    ((A, A, A, 0, None, 1, 1, 8, 8, 64, 0.1, 0), attn.ATTN_EINVAL),          # null o
+    ((A, A, A, 2 * A, None, -1, 1, 8, 8, 64, 0.1, 0), attn.ATTN_EINVAL),     # negative B
+    ((A, A, A, 2 * A, None, 1, 1, 8, 0, 64, 0.1, 0), attn.ATTN_EINVAL),      # Nk = 0
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 64, -0.5, 0), attn.ATTN_EINVAL),     # negative scale
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 64, float("nan"), 0), attn.ATTN_EINVAL),
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 96, 0.1, 0), attn.ATTN_EUNSUPPORTED),  # D
+    ((A + 2, A, A, 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0), attn.ATTN_EUNSUPPORTED),  # misaligned q
+    ((A, A, A, 2 * A, A + 2, 1, 1, 8, 8, 64, 0.1, 0), attn.ATTN_EUNSUPPORTED),  # misaligned lse
+    ((A, A, A, A, None, 1, 1, 8, 8, 64, 0.1, 0), attn.ATTN_EUNSUPPORTED),    # o overlaps q
+    ((A, A, A, 2 * A, None, 300, 300, 8, 8, 64, 0.1, 0), attn.ATTN_EUNSUPPORTED),  # B*H > 65535
+    ((A, A, A, 2 * A, None, 0, 4, 8, 8, 64, 0.1, 0), attn.ATTN_OK),          # empty: no-op
+    ((A, A, A, 2 * A, None, 2, 4, 0, 8, 64, 0.1, 1), attn.ATTN_OK),          # Nq = 0: no-op
+])
+def test_argument_validation_without_device(lib, args, code):
+    assert attn.attn_fwd(*args, None) == code
+
+
+def test_debug_hook_validation(lib):
+    assert attn.debug_set(0, -1) == attn.ATTN_EINVAL
+    assert attn.debug_set(10, -2) == attn.ATTN_EINVAL
+    assert attn.debug_set(2_000_000_000, -1) == attn.ATTN_OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        attn.fwd(x, x, x)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from attention_forward_12_gb300 import _binding
+    saved = _binding._lib
+    _binding._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            _binding.load_library(str(tmp_path / "nope.so"))
+    finally:
+        _binding._lib = saved
