@@ -8,36 +8,46 @@
 // running denominator, running unnormalised output -- across key/value
 // tiles, so the N x N scores never reach HBM (sections "Move 0" FA-1 and
 // "Move 1 -- Tensor Cores").  The page's kernels are mma.sync designs for
-// sm_120; this one is built for the datacenter Blackwell tensor core:
+// sm_120; this one is built for the datacenter Blackwell tensor core.
 //
-//   * TMA producer (warp 4): loads the Q tile once and streams K and V tiles
-//     through an NS-deep ring of 128B-swizzled shared-memory stages, each
-//     stage guarded by full/empty mbarriers ("New Hardware: TMA": rank-N box
+// One CTA owns two 128-row query tiles of one (batch, head) -- the
+// register-tiling idea of the page's "Move 4" (two independent (m, l, O)
+// chains sharing every K/V fragment), lifted to two warpgroups sharing every
+// K/V shared-memory tile:
+//
+//   * TMA producer (warp 8): loads both Q tiles once and streams K and V
+//     tiles through an NS-deep ring of 128B-swizzled shared-memory stages,
+//     each stage guarded by full/empty mbarriers ("New Hardware: TMA": box
 //     copies, hardware swizzle, one issuing thread, mbarrier transaction
-//     counts; "Move 3 -- Pipelining": prefetch tile j+1 under tile j).
-//   * MMA issuer (warp 5, one thread): S_j = Q K_j^T with tcgen05.mma
-//     (A and B from shared memory) into one of two TMEM score buffers, and
-//     O += P_j V_j with tcgen05.mma taking P from TMEM (the analogue of the
-//     page's C->A register repack: P never goes through shared memory).
-//     Double-buffered S lets S_{j+1} run on the tensor core while the
-//     softmax warps work on S_j.
-//   * Softmax warpgroup (warps 0-3, thread t owns query row t, which is
-//     TMEM lane t): reads S_j with tcgen05.ld, masks, takes the row maximum,
-//     computes p = 2^(s*scale*log2(e) - m) with the scale folded into one
-//     FFMA, rounds p to fp16 and writes it back over S_j, sums it into d.
-//     O is rescaled lazily: only when a row's maximum grows by more than
-//     kTau (in log2 units) over the reference it was using; otherwise p is
-//     taken against the stale reference, which is exact because p, d and o
-//     share it (the conditional rescale the page credits to FlashAttention-4
-//     in "Relationship to FA-3 and FA-4").  At the end it normalises O by d,
-//     writes fp16 O and fp32 LSE.
-//   * Causal (key j masked when j > i): a query tile visits only the key
-//     tiles up to its diagonal, and only the diagonal and the ragged last
+//     counts; "Move 3 -- Pipelining": prefetch under compute).
+//   * MMA issuer (warp 9, one thread): S_w = Q_w K_j^T with tcgen05.mma
+//     (A and B from shared memory) into TMEM buffer w, and O_w += P_w V_j
+//     with tcgen05.mma taking P_w from TMEM, where the softmax wrote it over
+//     S_w (the analogue of the page's C->A register repack: P never goes
+//     through shared memory).  Issue order per key tile j:
+//         O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
+//     so that one warpgroup's softmax runs while the tensor core works on
+//     the other's tile.
+//   * Softmax warpgroups w = 0, 1 (warps 4w..4w+3; thread t owns row t of
+//     query tile w, which is TMEM lane t): tcgen05.ld of S_w, mask, row
+//     maximum (3-input max), p = 2^(s*scale*log2(e) - m) with the scale
+//     folded into a packed FFMA2, packed row sums, fp16 pack of p written
+//     back over S_w.  O_w is rescaled lazily: only when a row's maximum grows
+//     by more than kTau (log2 units) over the reference it was using;
+//     otherwise p is taken against the stale reference, which is exact
+//     because p, d and o share it (the conditional rescale the page credits
+//     to FlashAttention-4 in "Relationship to FA-3 and FA-4").  At the end the
+//     warpgroup normalises O_w by d and writes fp16 O and fp32 LSE.
+//   * Causal (key j masked when j > i): each query tile visits only the key
+//     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
 //
+// TMEM (512 columns): S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+D),
+// O_1 [384,384+D).
+//
 // Every mbarrier wait is bounded (see WaitCtl): a wait that runs out raises
-// the CTA's abort flag and the device status word, the CTA drains its TMA
-// copies and tensor-core work in flight, frees its TMEM and exits.
+// the CTA's abort flag and the device status word; the CTA then drains its
+// TMA copies and tensor-core work in flight, frees its TMEM and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -55,10 +65,13 @@ using namespace attn_sm103;
 
 namespace {
 
-constexpr int kThreads = 192;   // 4 softmax warps + TMA warp + MMA warp
-constexpr int kBlockM = 128;    // query rows per tile (= TMEM lanes)
-constexpr int kBlockN = 128;    // keys per tile
-constexpr float kTau = 8.0f;    // lazy-rescale threshold, log2 units
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kBlockM = 128;           // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;           // keys per tile
+constexpr int kRowsPerCta = 2 * kBlockM;
+constexpr float kTau = 8.0f;           // lazy-rescale threshold, log2 units
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 fp16 (one swizzle column block)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -66,10 +79,29 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 template <int HD, int NS>
 struct Layout {
   static constexpr int kChunks = HD / 64;
-  static constexpr uint32_t kTileBytes = kBlockM * HD * 2;  // Q, K or V tile
-  static constexpr int kBars = 1 + 4 * NS + 2 + 2 + 1 + 1;
-  static constexpr size_t kSmem = 1024 + kTileBytes * (1 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
+  static constexpr uint32_t kTileBytes = kBlockM * HD * 2;  // one Q, K or V tile
+  static constexpr int kBars = 1 + 4 * NS + 2 + 2 + 2 + 1;
+  static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
 };
+
+// Key tiles query tile w of the CTA visits (0 if the tile lies past Nq).
+template <bool CAUSAL>
+__device__ __forceinline__ int tile_kv_count(int row0, int Nq, int Nk) {
+  if (row0 >= Nq) return 0;
+  const int kv_end = CAUSAL ? min(Nk, row0 + kBlockM) : Nk;
+  return (kv_end + kBlockN - 1) / kBlockN;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 }  // namespace
 
@@ -89,18 +121,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* sQ = sm;
-  uint8_t* sK = sQ + TB;
-  uint8_t* sV = sK + NS * TB;
+  uint8_t* sQ = sm;                 // 2 tiles
+  uint8_t* sK = sQ + 2 * TB;        // NS tiles
+  uint8_t* sV = sK + NS * TB;       // NS tiles
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sV + NS * TB);
   uint64_t* k_full = q_full + 1;
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
-  uint64_t* s_full = v_empty + NS;  // [2] S_j landed in TMEM buffer j&1
-  uint64_t* p_full = s_full + 2;    // [2] P_j written over S_j (and O rescaled)
-  uint64_t* o_done = p_full + 2;    // one phase per completed O += P V
-  uint64_t* drain = o_done + 1;     // abort path only
+  uint64_t* s_full = v_empty + NS;  // [2] S_w landed in TMEM
+  uint64_t* p_full = s_full + 2;    // [2] P_w written over S_w (and O_w rescaled)
+  uint64_t* o_done = p_full + 2;    // [2] one phase per completed O_w += P_w V
+  uint64_t* drain = o_done + 2;     // abort path only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* last_k = abort_flag + 1;     // [NS] last tile loaded per stage (abort drain)
@@ -109,10 +141,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
-  const int qt = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int r0 = qt * kBlockM;
-  const int kv_end = CAUSAL ? min(Nk, r0 + kBlockM) : Nk;
-  const int nkv = (kv_end + kBlockN - 1) / kBlockN;  // >= 1
+  const int pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int r0 = pair * kRowsPerCta;
+  const int nkv0 = tile_kv_count<CAUSAL>(r0, Nq, Nk);            // >= 1
+  const int nkv1 = tile_kv_count<CAUSAL>(r0 + kBlockM, Nq, Nk);  // 0 if tile 1 is past Nq
+  const int nkv = max(nkv0, nkv1);
 
   // A CTA of a launch that already recorded an error does no work: after a
   // timeout the remaining CTAs exit at once instead of each waiting out its
@@ -131,16 +164,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       last_k[s] = -1;
       last_v[s] = -1;
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], kBlockM);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&s_full[w], 1);
+      mbar_init(&p_full[w], kBlockM);
+      mbar_init(&o_done[w], 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -149,19 +182,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
 
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem;        // columns [0,128): S / P buffer 0
-  const uint32_t tS1 = tmem + 128;  // columns [128,256): S / P buffer 1
-  const uint32_t tO = tmem + 256;   // columns [256, 256+HD): O accumulator
   const WaitCtl wc{abort_flag, &g_attn_status, timeout_ns};
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(q_full, TB);
+      mbar_arrive_expect_tx(q_full, nkv1 > 0 ? 2 * TB : TB);
       for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * 64, r0, bh);
+      if (nkv1 > 0)
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sQ + TB + c * kChunkBytes, &tmQ, q_full, c * 64, r0 + kBlockM, bh);
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
         const int s = j % NS;
@@ -189,94 +222,113 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_f16_f32(kBlockM, kBlockN, false, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32(kBlockM, HD, false, true);
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(q_full, 0, wc, ATTN_ETIMEOUT);
-      if (ok) tc_fence_after();
-      for (int j = 0; j <= nkv && ok; ++j) {
-        if (j < nkv) {
-          // S_j = Q K_j^T : both operands K-major, 128B swizzle; K = HD in
-          // steps of 16 (32 bytes inside a 128-byte swizzle row).
-          const int s = j % NS;
-          ok = mbar_wait(&k_full[s], (j / NS) & 1, wc, ATTN_ETIMEOUT);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t dS = (j & 1) ? tS1 : tS0;
+      // S_w = Q_w K^T of stage s: both operands K-major, 128B swizzle; the
+      // reduction over D runs in steps of 16 (32 bytes inside a swizzle row).
+      auto issue_s = [&](int w, int s) {
+        const uint32_t dS = tmem + w * 128;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(dS, smem_desc(aQ + off, 16, 1024), smem_desc(aK + s * TB + off, 16, 1024), kIdescQK,
-                    kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&k_empty[s]);
-          umma_commit(&s_full[j & 1]);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          umma_ss(dS, smem_desc(aQ + w * TB + off, 16, 1024), smem_desc(aK + s * TB + off, 16, 1024), kIdescQK,
+                  kk > 0 ? 1u : 0u);
         }
-        if (j >= 1) {
-          // O += P_t V_t : P (fp16, packed two per column) from TMEM as the
-          // A operand, V from shared memory MN-major (rows = keys, 128 bytes
-          // of D per row; LBO = next 64 columns of D, SBO = next 8 keys).
-          const int t = j - 1;
-          const int s = t % NS;
-          ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, wc, ATTN_ETIMEOUT);
-          if (ok) ok = mbar_wait(&v_full[s], (t / NS) & 1, wc, ATTN_ETIMEOUT);
+        umma_commit(&s_full[w]);
+      };
+      // O_w += P_w V of stage s: P (fp16, two per column) from TMEM as the A
+      // operand; V MN-major in shared memory (rows = keys, 128 bytes of D per
+      // row; LBO = next 64 columns of D, SBO = next 8 keys).
+      auto issue_pv = [&](int w, int j, int s) -> bool {
+        if (!mbar_wait(&p_full[w], j & 1, wc, ATTN_ETIMEOUT)) return false;
+        tc_fence_after();
+        const uint32_t aP = tmem + w * 128;
+        const uint32_t dO = tmem + 256 + w * 128;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_ts(dO, aP + kk * 8, smem_desc(aV + s * TB + kk * 2048, kChunkBytes, 1024), kIdescPV,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&o_done[w]);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, wc, ATTN_ETIMEOUT) && mbar_wait(&k_full[0], 0, wc, ATTN_ETIMEOUT);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        if (nkv1 > 0) issue_s(1, 0);
+        umma_commit(&k_empty[0]);
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int s = j % NS;
+        const int s1 = (j + 1) % NS;
+        const bool more = j + 1 < nkv;
+        ok = mbar_wait(&v_full[s], (j / NS) & 1, wc, ATTN_ETIMEOUT);
+        if (!ok) break;
+        tc_fence_after();
+        if (j < nkv0 && !(ok = issue_pv(0, j, s))) break;
+        if (more) {
+          ok = mbar_wait(&k_full[s1], ((j + 1) / NS) & 1, wc, ATTN_ETIMEOUT);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t aP = (t & 1) ? tS1 : tS0;
-#pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            umma_ts(tO, aP + kk * 8, smem_desc(aV + s * TB + kk * 2048, kChunkBytes, 1024), kIdescPV,
-                    (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&v_empty[s]);
-          umma_commit(o_done);
+          if (j + 1 < nkv0) issue_s(0, s1);
+        }
+        if (j < nkv1 && !(ok = issue_pv(1, j, s))) break;
+        umma_commit(&v_empty[s]);
+        if (more) {
+          if (j + 1 < nkv1) issue_s(1, s1);
+          umma_commit(&k_empty[s1]);
         }
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int row = threadIdx.x;  // tile row == TMEM lane
-    const int i = r0 + row;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int wg = warp >> 2;             // query tile of this warpgroup
+    const int row = threadIdx.x & 127;    // tile row == TMEM lane
+    const int rw = r0 + wg * kBlockM;
+    const int i = rw + row;
+    const int my_nkv = wg ? nkv1 : nkv0;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + wg * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + wg * 128 + lane_off;
     const int row_lim = CAUSAL ? min(Nk, i + 1) : Nk;  // admissible keys: [0, row_lim)
+    const float2 sl2v = make_float2(sl2, sl2);
     float m_ref = -INFINITY;  // reference maximum, log2 units of the scaled score
     float dsum = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const uint32_t tS = (j & 1) ? tS1 : tS0;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, wc, ATTN_ETIMEOUT));
+    for (int j = 0; j < my_nkv; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], j & 1, wc, ATTN_ETIMEOUT));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
 
       const int key0 = j * kBlockN;
-      const bool masked = (key0 + kBlockN > Nk) || (CAUSAL && key0 + kBlockN - 1 > r0);
+      const bool masked = (key0 + kBlockN > Nk) || (CAUSAL && key0 + kBlockN - 1 > rw);
       const int lim = row_lim - key0;  // columns [0, lim) of this tile are admissible
-      float mx = -INFINITY;
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const bool valid = (c * 32 + e) < lim;
-            const float x = valid ? __uint_as_float(sr[c][e]) : -INFINITY;
-            sr[c][e] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
       }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 8)
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            mx4[a] = max3(mx4[a], __uint_as_float(sr[c][e + 2 * a]), __uint_as_float(sr[c][e + 2 * a + 1]));
+      const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
       const float mt = (mx == -INFINITY) ? -INFINITY : mx * sl2;
       const bool resc = mt > m_ref + kTau;
       float alpha = 1.f;
@@ -286,79 +338,91 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         dsum *= alpha;
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const float2 nm = make_float2(neg_m, neg_m);
 
-      // p = 2^(s*sl2 - m_ref), rounded to fp16 precision in fp32 so that the
-      // denominator sums exactly the weights the tensor core multiplies V by.
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[2][32];
+      // p = 2^(s*sl2 - m_ref); P goes back over S as fp16 pairs.
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, neg_m));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, neg_m));
-          if (masked) {
-            p0 = (c * 32 + e) < lim ? p0 : 0.f;
-            p1 = (c * 32 + e + 1) < lim ? p1 : 0.f;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * h + cc;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
+                                        sl2v, nm);
+            float p0 = ex2_approx(x.x);
+            float p1 = ex2_approx(x.y);
+            if (masked) {  // -inf * 0 is NaN when scale == 0: select explicitly
+              p0 = (c * 32 + e < lim) ? p0 : 0.f;
+              p1 = (c * 32 + e + 1 < lim) ? p1 : 0.f;
+            }
+            acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], make_float2(p0, p1));
+            pk[cc * 16 + (e >> 1)] = pack_half2(p0, p1);
           }
-          p0 = __uint_as_float((__float_as_uint(p0) + 0x1000u) & 0xFFFFE000u);
-          p1 = __uint_as_float((__float_as_uint(p1) + 0x1000u) & 0xFFFFE000u);
-          rs0 += p0;
-          rs1 += p1;
-          const __half2 h2 = __floats2half2_rn(p0, p1);
-          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-      dsum += rs0 + rs1;
-      tmem_st32(tS + lane_off, pk[0]);
-      tmem_st32(tS + lane_off + 32, pk[1]);
+        tmem_st32(tS + h * 32, pk);
+      }
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      dsum += a.x + a.y;
 
       if (j >= 1) {
-        // O must hold exactly P_0..P_{j-1} before it is rescaled and before
-        // P_j is released; every completion of O += P V is observed in order.
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, wc, ATTN_ETIMEOUT));
+        // O_w must hold exactly P_0..P_{j-1} before it is rescaled and before
+        // P_j is released; every completion of O_w += P_w V is observed in order.
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT));
         if (!ok) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, resc)) {
+          const float2 al = make_float2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t orr[32];
-            tmem_ld32(tO + lane_off + c * 32, orr);
+            tmem_ld32(tO + c * 32, orr);
             tmem_ld_wait(orr);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, orr);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
+              orr[e] = __float_as_uint(v.x);
+              orr[e + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + c * 32, orr);
           }
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive(&p_full[wg]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (nkv - 1) & 1, wc, ATTN_ETIMEOUT));
-    if (ok) {
+    if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (my_nkv - 1) & 1, wc, ATTN_ETIMEOUT));
+    if (ok && my_nkv > 0) {
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
       const float inv = 1.f / dsum;
+      const float2 iv = make_float2(inv, inv);
       __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t orr[32];
-        tmem_ld32(tO + lane_off + c * 32, orr);
+        tmem_ld32(tO + c * 32, orr);
         tmem_ld_wait(orr);
         if (i < Nq) {
           uint32_t h[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const __half2 h2 = __floats2half2_rn(__uint_as_float(orr[2 * e]) * inv,
-                                                 __uint_as_float(orr[2 * e + 1]) * inv);
-            h[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1])), iv);
+            h[e] = pack_half2(v.x, v.y);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
         }
       }
-      if (lse != nullptr && i < Nq) lse[static_cast<size_t>(bh) * Nq + i] = (m_ref + log2f(dsum)) * 0.69314718055994531f;
+      if (lse != nullptr && i < Nq)
+        lse[static_cast<size_t>(bh) * Nq + i] = (m_ref + log2f(dsum)) * 0.69314718055994531f;
     }
   }
 
@@ -367,21 +431,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (*abort_flag) {
     // A wait ran out somewhere in this CTA: let every TMA copy and every
     // tensor-core op it issued land before the shared memory and TMEM go.
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
       mbar_wait(q_full, 0, wc, ATTN_ETIMEOUT, false);
       for (int s = 0; s < NS; ++s) {
         if (last_k[s] >= 0) mbar_wait(&k_full[s], (last_k[s] / NS) & 1, wc, ATTN_ETIMEOUT, false);
         if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / NS) & 1, wc, ATTN_ETIMEOUT, false);
       }
     }
-    if (warp == 5 && lane == 0) {
+    if (warp == kMmaWarp && lane == 0) {
       umma_commit(drain);
       mbar_wait(drain, 0, wc, ATTN_ETIMEOUT, false);
     }
     tc_fence_before();
     __syncthreads();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -444,7 +508,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
       cudaSuccess)
     return ATTN_ECUDA;
-  dim3 grid((Nq + kBlockM - 1) / kBlockM, BH, 1);
+  dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, 1);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, Nq, Nk, sl2, timeout_ns, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
