@@ -27,12 +27,16 @@
 //     through shared memory).  Issue order per key tile j:
 //         O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
 //     so that one warpgroup's softmax runs while the tensor core works on
-//     the other's tile.
+//     the other's tile.  With SPLIT_P (used at D=64, where the row update
+//     outweighs the matmuls) each O_w += P_w V_j is issued in two halves of
+//     64 keys: the first as soon as the softmax has released the first half
+//     of P_w, overlapping the second half's exponentials.
 //   * Softmax warpgroups w = 0, 1 (warps 4w..4w+3; thread t owns row t of
 //     query tile w, which is TMEM lane t): tcgen05.ld of S_w, mask, row
 //     maximum (3-input max), p = 2^(s*scale*log2(e) - m) with the scale
 //     folded into a packed FFMA2, packed row sums, fp16 pack of p written
-//     back over S_w.  O_w is rescaled lazily: only when a row's maximum grows
+//     back over S_w (in two released halves with SPLIT_P).  O_w is rescaled
+//     lazily, before the tile's P is released: only when a row's maximum grows
 //     by more than kTau (log2 units) over the reference it was using;
 //     otherwise p is taken against the stale reference, which is exact
 //     because p, d and o share it (the conditional rescale the page credits
@@ -75,12 +79,15 @@ constexpr float kTau = 8.0f;           // lazy-rescale threshold, log2 units
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 fp16 (one swizzle column block)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// Exponentials sent to the FMA-pipe polynomial: one pair in kEmu (0 = none).
+constexpr int kEmu64 = 0;
+constexpr int kEmu128 = 0;
 
 template <int HD, int NS>
 struct Layout {
   static constexpr int kChunks = HD / 64;
   static constexpr uint32_t kTileBytes = kBlockM * HD * 2;  // one Q, K or V tile
-  static constexpr int kBars = 1 + 4 * NS + 2 + 2 + 2 + 1;
+  static constexpr int kBars = 1 + 4 * NS + 2 + 2 + 2 + 2 + 1;
   static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
 };
 
@@ -109,7 +116,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // recorded since the last attn_get_status().
 __device__ int g_attn_status;
 
-template <int HD, bool CAUSAL, int NS>
+template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
@@ -130,7 +137,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
   uint64_t* s_full = v_empty + NS;  // [2] S_w landed in TMEM
-  uint64_t* p_full = s_full + 2;    // [2] P_w written over S_w (and O_w rescaled)
+  uint64_t* p_half = s_full + 2;    // [2] first 64 columns of P_w written (and O_w rescaled)
+  uint64_t* p_full = p_half + 2;    // [2] all of P_w written over S_w
   uint64_t* o_done = p_full + 2;    // [2] one phase per completed O_w += P_w V
   uint64_t* drain = o_done + 2;     // abort path only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -166,6 +174,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&s_full[w], 1);
+      mbar_init(&p_half[w], kBlockM);
       mbar_init(&p_full[w], kBlockM);
       mbar_init(&o_done[w], 1);
     }
@@ -242,16 +251,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       };
       // O_w += P_w V of stage s: P (fp16, two per column) from TMEM as the A
       // operand; V MN-major in shared memory (rows = keys, 128 bytes of D per
-      // row; LBO = next 64 columns of D, SBO = next 8 keys).
+      // row; LBO = next 64 columns of D, SBO = next 8 keys).  The first 64 keys
+      // go as soon as the softmax has released the first half of P, so the
+      // tensor core works while the second half is being computed.
       auto issue_pv = [&](int w, int j, int s) -> bool {
-        if (!mbar_wait(&p_full[w], j & 1, wc, ATTN_ETIMEOUT)) return false;
-        tc_fence_after();
         const uint32_t aP = tmem + w * 128;
         const uint32_t dO = tmem + 256 + w * 128;
+        constexpr int kParts = SPLIT_P ? 2 : 1;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_ts(dO, aP + kk * 8, smem_desc(aV + s * TB + kk * 2048, kChunkBytes, 1024), kIdescPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+        for (int part = 0; part < kParts; ++part) {
+          const bool last = part == kParts - 1;
+          if (!mbar_wait(last ? &p_full[w] : &p_half[w], j & 1, wc, ATTN_ETIMEOUT)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = part * 8 / kParts; kk < (part + 1) * 8 / kParts; ++kk)
+            umma_ts(dO, aP + kk * 8, smem_desc(aV + s * TB + kk * 2048, kChunkBytes, 1024), kIdescPV,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
         umma_commit(&o_done[w]);
         return true;
       };
@@ -299,6 +315,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float2 sl2v = make_float2(sl2, sl2);
     float m_ref = -INFINITY;  // reference maximum, log2 units of the scaled score
     float dsum = 0.f;
+    // O_w must hold exactly P_0..P_{j-1} before it is rescaled and before
+    // P_j is released; every completion of O_w += P_w V is observed in order
+    // (in steady state it completed long ago).  The rescale itself is rare
+    // (lazy) and works in 8-column chunks so that it stays light on registers
+    // while the 128-column score row may still be live.
+    auto rescale_o = [&](int j, bool resc, float alpha) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT))) return false;
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, resc)) {
+        const float2 al = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int c = 0; c < HD / 8; ++c) {
+          uint32_t orr[8];
+          tmem_ld8(tO + c * 8, orr);
+          tmem_ld_wait8(orr);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
+            orr[e] = __float_as_uint(v.x);
+            orr[e + 1] = __float_as_uint(v.y);
+          }
+          tmem_st8(tO + c * 8, orr);
+        }
+      }
+      return true;
+    };
     bool ok = true;
     for (int j = 0; j < my_nkv; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], j & 1, wc, ATTN_ETIMEOUT));
@@ -337,10 +379,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         m_ref = mt;
         dsum *= alpha;
       }
+      if constexpr (SPLIT_P) {
+        if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
+      }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const float2 nm = make_float2(neg_m, neg_m);
 
-      // p = 2^(s*sl2 - m_ref); P goes back over S as fp16 pairs.
+      // p = 2^(s*sl2 - m_ref); P goes back over S as fp16 pairs, in two
+      // halves of 64 keys, each released to the MMA thread as soon as it is
+      // in TMEM.
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
 #pragma unroll
@@ -353,8 +400,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           for (int e = 0; e < 32; e += 2) {
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
                                         sl2v, nm);
-            float p0 = ex2_approx(x.x);
-            float p1 = ex2_approx(x.y);
+            float p0, p1;
+            if (EMU > 0 && (e >> 1) % (EMU > 0 ? EMU : 1) == (EMU > 0 ? EMU : 1) - 1) {
+              const float2 pp = exp2_poly2(x);  // one pair in EMU on the FMA pipe
+              p0 = pp.x;
+              p1 = pp.y;
+            } else {
+              p0 = ex2_approx(x.x);
+              p1 = ex2_approx(x.y);
+            }
             if (masked) {  // -inf * 0 is NaN when scale == 0: select explicitly
               p0 = (c * 32 + e < lim) ? p0 : 0.f;
               p1 = (c * 32 + e + 1 < lim) ? p1 : 0.f;
@@ -364,38 +418,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
         tmem_st32(tS + h * 32, pk);
+        if constexpr (SPLIT_P) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(h ? &p_full[wg] : &p_half[wg]);
+        }
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]);
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 a = __fadd2_rn(a01, a23);
       dsum += a.x + a.y;
-
-      if (j >= 1) {
-        // O_w must hold exactly P_0..P_{j-1} before it is rescaled and before
-        // P_j is released; every completion of O_w += P_w V is observed in order.
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-          const float2 al = make_float2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(tO + c * 32, orr);
-            tmem_ld_wait(orr);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
-              orr[e] = __float_as_uint(v.x);
-              orr[e + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(tO + c * 32, orr);
-          }
-        }
+      if constexpr (!SPLIT_P) {
+        if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[wg]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[wg]);
     }
     if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (my_nkv - 1) & 1, wc, ATTN_ETIMEOUT));
     if (ok && my_nkv > 0) {
@@ -499,11 +537,11 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-template <int HD, bool CAUSAL, int NS>
+template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse, int BH,
            int Nq, int Nk, float sl2, cudaStream_t st, uint64_t timeout_ns, int drop) {
   using L = Layout<HD, NS>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL, NS>;
+  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
       cudaSuccess)
@@ -563,10 +601,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   const float sl2 = scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (D == 64)
-    return causal ? launch<64, true, 4>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop)
-                  : launch<64, false, 4>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop);
-  return causal ? launch<128, true, 2>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop)
-                : launch<128, false, 2>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop);
+    return causal ? launch<64, true, 4, true, kEmu64>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop)
+                  : launch<64, false, 4, true, kEmu64>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop);
+  return causal ? launch<128, true, 2, false, kEmu128>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop)
+                : launch<128, false, 2, false, kEmu128>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop);
 }
 
 const char* attn_strerror(int code) {

@@ -27,7 +27,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from attention_forward_12_gb300 import synth  # noqa: E402
+from attention_forward_12_gb300 import multirank, synth  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s and µs/call at 1 GB300; % of dense FP16 tensor peak"
 UNIT = "TFLOP/s"
@@ -233,8 +233,10 @@ def main():
     torch.cuda.set_device(dev)
     attn.load_library()
 
-    # inputs: seeded on the host (the same bytes the oracle sees), copied once
-    qn, kn, vn = synth.workload_qkv(w)
+    # inputs: seeded on the host (the same bytes the oracle sees), copied once;
+    # every rank draws its own independent problems of the workload's shape
+    qn, kn, vn = synth.make_qkv(w.B, w.H, w.Nq, w.Nk, w.D, multirank.rank_seed(w.seed, rank),
+                                w.sigma_qk, w.sigma_v)
     q = torch.from_numpy(qn).to(dev)
     k = torch.from_numpy(kn).to(dev)
     v = torch.from_numpy(vn).to(dev)
@@ -292,12 +294,9 @@ def main():
         step_ms = statistics.mean(kernel_ms)
     else:
         step_ms = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = multirank.max_over_ranks(step_ms, dist, dev)
     f = flops(w)
-    value = world * f / (step_ms * 1e-3) / 1e12
+    value = multirank.aggregate_tflops(f, world, step_ms)
     kern_avg_ms = statistics.mean(kernel_ms)
 
     # ---------------- end to end: host buffers, copies inside the timed region
@@ -329,11 +328,8 @@ def main():
         b.record(stream)
         barrier()
         e_ms = a.elapsed_time(b) / n_e2e
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * f / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+        e_ms = multirank.max_over_ranks(e_ms, dist, dev)
+        e2e = {"value": multirank.aggregate_tflops(f, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "steps": n_e2e,
                "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
                "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4)}
