@@ -16,7 +16,8 @@ from ._build import LIB_PATH
 ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = 0, 1, 2, 3, 4
 
 # Every symbol the C header declares; the CPU tests check they are exported.
-EXPORTS = ("attn_fwd", "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
+EXPORTS = ("attn_fwd", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
+           "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -42,6 +43,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd.restype = i32
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, vp]
+            lib.attn_fwd_splitkv.restype = i32
+            lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                             ctypes.c_float, i32, i32, vp, ctypes.c_size_t, vp]
+            lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            lib.attn_splitkv_suggest.restype = i32
+            lib.attn_splitkv_suggest.argtypes = [i32, i32, i32, i32, i32, i32]
             lib.attn_strerror.restype = ctypes.c_char_p
             lib.attn_strerror.argtypes = [i32]
             lib.attn_get_status.restype = i32
@@ -65,6 +73,23 @@ def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None
     return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
                                    int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
                                    stream)
+
+
+def attn_fwd_splitkv(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None,
+                     B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+                     num_splits: int, ws_ptr: int | None, ws_bytes: int, stream: int | None) -> int:
+    """Direct call of the split-KV entry point with raw device pointers."""
+    return load_library().attn_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq),
+                                           int(Nk), int(D), float(scale), int(bool(causal)),
+                                           int(num_splits), ws_ptr, int(ws_bytes), stream)
+
+
+def splitkv_workspace_bytes(B: int, H: int, Nq: int, D: int, num_splits: int) -> int:
+    return int(load_library().attn_splitkv_workspace_bytes(int(B), int(H), int(Nq), int(D), int(num_splits)))
+
+
+def splitkv_suggest(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool) -> int:
+    return int(load_library().attn_splitkv_suggest(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal))))
 
 
 def _current_stream_ptr(device) -> int:
@@ -101,6 +126,41 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse
                     _current_stream_ptr(q.device))
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd")
+    return out, lse
+
+
+def fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, num_splits: int | None = None,
+                workspace=None, out=None, lse=None, want_lse: bool = True):
+    """Split-KV forward (see attn.h); returns (o, lse).  num_splits defaults
+    to the library's suggestion; the workspace is allocated with torch when
+    not given (a uint8 CUDA tensor of at least splitkv_workspace_bytes)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float16):
+            raise TypeError(f"{name} must be a CUDA float16 tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D [B,H,N,D] tensor")
+    B, H, Nq, D = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError("k and v must be [B,H,Nk,D] with q's B, H and D")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if num_splits is None:
+        num_splits = max(1, splitkv_suggest(B, H, Nq, Nk, D, causal))
+    need = splitkv_workspace_bytes(B, H, Nq, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    code = attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, D, scale, causal,
+                            num_splits, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _current_stream_ptr(q.device))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_splitkv")
     return out, lse
 
 

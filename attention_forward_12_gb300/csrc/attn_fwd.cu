@@ -116,11 +116,12 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // recorded since the last attn_get_status().
 __device__ int g_attn_status;
 
-template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU>
+template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
-                float* __restrict__ lse, int Nq, int Nk, float sl2, uint64_t timeout_ns,
+                float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_l, int Nq, int Nk,
+                float sl2, uint64_t timeout_ns,
                 int drop_tile) {
   using L = Layout<HD, NS>;
   constexpr uint32_t TB = L::kTileBytes;
@@ -151,9 +152,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int bh = blockIdx.y;
   const int pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
   const int r0 = pair * kRowsPerCta;
-  const int nkv0 = tile_kv_count<CAUSAL>(r0, Nq, Nk);            // >= 1
-  const int nkv1 = tile_kv_count<CAUSAL>(r0 + kBlockM, Nq, Nk);  // 0 if tile 1 is past Nq
+  // Key tiles of this CTA: all of the pair's (grid z = 1), or with split-KV
+  // the contiguous share [t0, t1) of split blockIdx.z.  nkv0 / nkv1 count the
+  // tiles each query tile visits in that share (0 if the tile lies past Nq
+  // or, when causal, if its diagonal comes before the share).
+  const int nkv0_all = tile_kv_count<CAUSAL>(r0, Nq, Nk);
+  const int nkv1_all = tile_kv_count<CAUSAL>(r0 + kBlockM, Nq, Nk);
+  const int nkv_all = max(nkv0_all, nkv1_all);
+  const int t0 = SPLITKV ? static_cast<int>(static_cast<int64_t>(nkv_all) * blockIdx.z / gridDim.z) : 0;
+  const int t1 = SPLITKV ? static_cast<int>(static_cast<int64_t>(nkv_all) * (blockIdx.z + 1) / gridDim.z) : nkv_all;
+  const int nkv0 = SPLITKV ? max(0, min(t1, nkv0_all) - t0) : nkv0_all;
+  const int nkv1 = SPLITKV ? max(0, min(t1, nkv1_all) - t0) : nkv1_all;
   const int nkv = max(nkv0, nkv1);
+  const size_t rows_total = static_cast<size_t>(gridDim.y) * Nq;  // split-KV part stride
 
   // A CTA of a launch that already recorded an error does no work: after a
   // timeout the remaining CTAs exit at once instead of each waiting out its
@@ -161,6 +172,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) *abort_flag = *static_cast<volatile int*>(&g_attn_status);
   __syncthreads();
   if (*abort_flag) return;
+  if constexpr (SPLITKV) {
+    if (nkv == 0) {
+      // No admissible key in this share for either tile: an empty part
+      // (O = 0, LSE = -inf), which the merge gives zero weight.
+      const int i = r0 + static_cast<int>(threadIdx.x);
+      if (threadIdx.x < kRowsPerCta && i < Nq) {
+        const size_t rr = static_cast<size_t>(blockIdx.z) * rows_total + static_cast<size_t>(bh) * Nq + i;
+        float4* dst = reinterpret_cast<float4*>(ws_o + rr * HD);
+#pragma unroll 4
+        for (int e = 0; e < HD / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ws_l[rr] = -INFINITY;
+      }
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -199,8 +225,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(q_full, nkv1 > 0 ? 2 * TB : TB);
-      for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * 64, r0, bh);
+      mbar_arrive_expect_tx(q_full, (nkv0 > 0 ? TB : 0) + (nkv1 > 0 ? TB : 0));
+      if (nkv0 > 0)
+        for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * 64, r0, bh);
       if (nkv1 > 0)
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sQ + TB + c * kChunkBytes, &tmQ, q_full, c * 64, r0 + kBlockM, bh);
@@ -213,14 +240,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (j != drop_tile) {  // drop_tile >= 0 only under attn_debug_set
           mbar_arrive_expect_tx(&k_full[s], TB);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(sK + s * TB + c * kChunkBytes, &tmK, &k_full[s], c * 64, j * kBlockN, bh);
+            tma_load_3d(sK + s * TB + c * kChunkBytes, &tmK, &k_full[s], c * 64, (t0 + j) * kBlockN, bh);
           last_k[s] = j;
         }
         if (j >= NS) ok = mbar_wait(&v_empty[s], ph ^ 1, wc, ATTN_ETIMEOUT);
         if (!ok) break;
         mbar_arrive_expect_tx(&v_full[s], TB);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + s * TB + c * kChunkBytes, &tmV, &v_full[s], c * 64, j * kBlockN, bh);
+          tma_load_3d(sV + s * TB + c * kChunkBytes, &tmV, &v_full[s], c * 64, (t0 + j) * kBlockN, bh);
         last_v[s] = j;
       }
       // Tail: wait until the tensor core has released every stage, so that
@@ -274,7 +301,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       bool ok = mbar_wait(q_full, 0, wc, ATTN_ETIMEOUT) && mbar_wait(&k_full[0], 0, wc, ATTN_ETIMEOUT);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
+        if (nkv0 > 0) issue_s(0, 0);
         if (nkv1 > 0) issue_s(1, 0);
         umma_commit(&k_empty[0]);
       }
@@ -352,7 +379,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
 
-      const int key0 = j * kBlockN;
+      const int key0 = (t0 + j) * kBlockN;
       const bool masked = (key0 + kBlockN > Nk) || (CAUSAL && key0 + kBlockN - 1 > rw);
       const int lim = row_lim - key0;  // columns [0, lim) of this tile are admissible
       if (masked) {
@@ -436,7 +463,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
     }
     if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (my_nkv - 1) & 1, wc, ATTN_ETIMEOUT));
-    if (ok && my_nkv > 0) {
+    if (ok && my_nkv > 0 && !SPLITKV) {
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
       const float inv = 1.f / dsum;
@@ -461,6 +488,34 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (lse != nullptr && i < Nq)
         lse[static_cast<size_t>(bh) * Nq + i] = (m_ref + log2f(dsum)) * 0.69314718055994531f;
+    }
+    if (ok && SPLITKV) {
+      // ------------------------------------------- split-KV part epilogue
+      // This share's carrier, normalised: O_s = o / d in fp32 and its
+      // log-sum-exp in log2 units (-inf when the share has no admissible key
+      // for this tile); the merge kernel combines the shares.
+      if (my_nkv > 0) tc_fence_after();
+      const float inv = my_nkv > 0 ? 1.f / dsum : 0.f;
+      const size_t rr = static_cast<size_t>(blockIdx.z) * rows_total + static_cast<size_t>(bh) * Nq + i;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t orr[32];
+        if (my_nkv > 0) {
+          tmem_ld32(tO + c * 32, orr);
+          tmem_ld_wait(orr);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orr[e] = 0u;
+        }
+        if (i < Nq) {
+          float4* dst = reinterpret_cast<float4*>(ws_o + rr * HD + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(orr[4 * e]) * inv, __uint_as_float(orr[4 * e + 1]) * inv,
+                                 __uint_as_float(orr[4 * e + 2]) * inv, __uint_as_float(orr[4 * e + 3]) * inv);
+        }
+      }
+      if (i < Nq) ws_l[rr] = my_nkv > 0 ? m_ref + log2f(dsum) : -INFINITY;
     }
   }
 
@@ -487,6 +542,56 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Merge of the split-KV parts: the carrier merge of partial states
+// (m1,d1,o1) (+) (m2,d2,o2), applied to normalised parts.  For one row, with
+// l_s each part's log-sum-exp in log2 units and O_s its normalised output,
+//   m = max_s l_s,  w_s = 2^(l_s - m),  O = sum_s w_s O_s / sum_s w_s,
+//   LSE = ln2 * (m + log2 sum_s w_s).
+// An empty part has l_s = -inf and weight 0.  One warp per row; lane t owns
+// HD/32 consecutive columns, so every load of a part's row is coalesced.
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_l,
+                          __half* __restrict__ out, float* __restrict__ lse, size_t rows, int splits) {
+  constexpr int kPer = HD / 32;
+  const size_t row = static_cast<size_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < splits; ++s) m = fmaxf(m, ws_l[static_cast<size_t>(s) * rows + row]);
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float den = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < splits; ++s) {
+      const size_t rr = static_cast<size_t>(s) * rows + row;
+      const float w = ex2_approx(ws_l[rr] - m);
+      den += w;
+      const float* src = ws_o + rr * HD + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+        acc[2] += w * x.z;
+        acc[3] += w * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __half* dst = out + row * HD + lane * kPer;
+  if constexpr (kPer == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_half2(acc[0] * inv, acc[1] * inv), pack_half2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lse != nullptr && lane == 0) lse[row] = den > 0.f ? (m + log2f(den)) * 0.69314718055994531f : -INFINITY;
 }
 
 // =====================================================================
@@ -537,17 +642,98 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU>
-int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse, int BH,
-           int Nq, int Nk, float sl2, cudaStream_t st, uint64_t timeout_ns, int drop) {
+template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV>
+int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
+               float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
+               uint64_t timeout_ns, int drop) {
   using L = Layout<HD, NS>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU>;
+  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
       cudaSuccess)
     return ATTN_ECUDA;
-  dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, 1);
-  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, Nq, Nk, sl2, timeout_ns, drop);
+  dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, splits);
+  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
+                                         timeout_ns, drop);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
+}
+
+template <bool SPLITKV>
+int dispatch_fwd(int D, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                 void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
+                 cudaStream_t st, uint64_t timeout, int drop) {
+  if (D == 64)
+    return causal ? launch_fwd<64, true, 4, true, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+                                                                   splits, st, timeout, drop)
+                  : launch_fwd<64, false, 4, true, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                                                                    sl2, splits, st, timeout, drop);
+  return causal ? launch_fwd<128, true, 2, false, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                                                                    sl2, splits, st, timeout, drop)
+                : launch_fwd<128, false, 2, false, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                                                                     sl2, splits, st, timeout, drop);
+}
+
+// Argument checks shared by the forward entry points (no CUDA call).
+// Returns ATTN_OK with *empty set when there is nothing to compute.
+int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
+               int Nq, int Nk, int D, float scale, bool* empty) {
+  *empty = false;
+  if (!q || !k || !v || !o) return ATTN_EINVAL;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return ATTN_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_EINVAL;
+  if (D != 64 && D != 128) return ATTN_EUNSUPPORTED;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_EUNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535) return ATTN_EUNSUPPORTED;
+  if (B == 0 || H == 0 || Nq == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  const int BH = B * H;
+  const size_t qbytes = static_cast<size_t>(BH) * Nq * D * 2, kvbytes = static_cast<size_t>(BH) * Nk * D * 2;
+  if (ranges_overlap(o, qbytes, q, qbytes) || ranges_overlap(o, qbytes, k, kvbytes) ||
+      ranges_overlap(o, qbytes, v, kvbytes))
+    return ATTN_EUNSUPPORTED;
+  const size_t lbytes = static_cast<size_t>(BH) * Nq * 4;
+  if (lse && (ranges_overlap(lse, lbytes, o, qbytes) || ranges_overlap(lse, lbytes, q, qbytes) ||
+              ranges_overlap(lse, lbytes, k, kvbytes) || ranges_overlap(lse, lbytes, v, kvbytes)))
+    return ATTN_EUNSUPPORTED;
+  return ATTN_OK;
+}
+
+// The current device must be an sm_103 part; returns its SM count or <= 0.
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -ATTN_ECUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev_ready[dev] == 0) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return -ATTN_ECUDA;
+    g_dev_ready[dev] = (prop.major == 10 && prop.minor == 3) ? prop.multiProcessorCount : -1;
+  }
+  return g_dev_ready[dev] > 0 ? g_dev_ready[dev] : -ATTN_EUNSUPPORTED;
+}
+
+void debug_settings(uint64_t* timeout, int* drop) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  *timeout = g_timeout_ns;
+  *drop = g_drop_tile;
+}
+
+constexpr int kMaxSplits = 256;
+
+size_t splitkv_bytes(int B, int H, int Nq, int D, int splits) {
+  return static_cast<size_t>(splits) * B * H * Nq * (D + 1) * sizeof(float);
+}
+
+template <int HD>
+int launch_merge(const float* ws_o, const float* ws_l, void* o, float* lse, size_t rows, int splits,
+                 cudaStream_t st) {
+  const size_t blocks = (rows + 3) / 4;
+  if (blocks > 0x7fffffffu) return ATTN_EUNSUPPORTED;
+  attn_splitkv_merge_kernel<HD><<<static_cast<unsigned>(blocks), 128, 0, st>>>(
+      ws_o, ws_l, static_cast<__half*>(o), lse, rows, splits);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
@@ -557,54 +743,75 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
              int D, float scale, int causal, void* stream) {
-  if (!q || !k || !v || !o) return ATTN_EINVAL;
-  if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return ATTN_EINVAL;
-  if (!std::isfinite(scale) || scale < 0.f) return ATTN_EINVAL;
-  if (D != 64 && D != 128) return ATTN_EUNSUPPORTED;
-  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-  if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_EUNSUPPORTED;
-  if (static_cast<int64_t>(B) * H > 65535) return ATTN_EUNSUPPORTED;
-  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;  // empty output: nothing to do
+  bool empty = false;
+  const int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  const int sms = device_sms();
+  if (sms <= 0) return -sms;
   const int BH = B * H;
-  const size_t qbytes = static_cast<size_t>(BH) * Nq * D * 2, kvbytes = static_cast<size_t>(BH) * Nk * D * 2;
-  if (ranges_overlap(o, qbytes, q, qbytes) || ranges_overlap(o, qbytes, k, kvbytes) ||
-      ranges_overlap(o, qbytes, v, kvbytes))
-    return ATTN_EUNSUPPORTED;
-  if (lse && (ranges_overlap(lse, static_cast<size_t>(BH) * Nq * 4, o, qbytes) ||
-              ranges_overlap(lse, static_cast<size_t>(BH) * Nq * 4, q, qbytes) ||
-              ranges_overlap(lse, static_cast<size_t>(BH) * Nq * 4, k, kvbytes) ||
-              ranges_overlap(lse, static_cast<size_t>(BH) * Nq * 4, v, kvbytes)))
-    return ATTN_EUNSUPPORTED;
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_dev_ready[dev] == 0) {
-      cudaDeviceProp prop;
-      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_ECUDA;
-      g_dev_ready[dev] = (prop.major == 10 && prop.minor == 3) ? 1 : -1;
-    }
-    if (g_dev_ready[dev] < 0) return ATTN_EUNSUPPORTED;
-  }
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
     return ATTN_ECUDA;
   uint64_t timeout;
   int drop;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    timeout = g_timeout_ns;
-    drop = g_drop_tile;
-  }
+  debug_settings(&timeout, &drop);
   const float sl2 = scale * 1.4426950408889634f;
+  return dispatch_fwd<false>(D, causal, mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk, sl2, 1,
+                             static_cast<cudaStream_t>(stream), timeout, drop);
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits) {
+  if (B < 0 || H < 0 || Nq < 0 || (D != 64 && D != 128) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_bytes(B, H, Nq, D, num_splits);
+}
+
+int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (D != 64 && D != 128)) return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  const int64_t ctas = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
+  const int key_tiles = (causal ? std::min(Nk, kRowsPerCta * ((Nq + kRowsPerCta - 1) / kRowsPerCta)) : Nk);
+  const int tiles = (key_tiles + kBlockN - 1) / kBlockN;
+  int64_t s = (sms + ctas - 1) / ctas;             // fill the SMs once
+  s = std::min<int64_t>(s, std::max(1, tiles / 4));  // at least 4 key tiles per share
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits)));
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                     int Nk, int D, float scale, int causal, int num_splits, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  const int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_EINVAL;
+  if (empty) return ATTN_OK;
+  const size_t need = splitkv_bytes(B, H, Nq, D, num_splits);
+  if (!workspace || workspace_bytes < need) return ATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_EUNSUPPORTED;
+  const int BH = B * H;
+  const size_t qbytes = static_cast<size_t>(BH) * Nq * D * 2, kvbytes = static_cast<size_t>(BH) * Nk * D * 2;
+  if (ranges_overlap(workspace, need, q, qbytes) || ranges_overlap(workspace, need, k, kvbytes) ||
+      ranges_overlap(workspace, need, v, kvbytes) || ranges_overlap(workspace, need, o, qbytes) ||
+      (lse && ranges_overlap(workspace, need, lse, static_cast<size_t>(BH) * Nq * 4)))
+    return ATTN_EUNSUPPORTED;
+  const int sms = device_sms();
+  if (sms <= 0) return -sms;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
+    return ATTN_ECUDA;
+  uint64_t timeout;
+  int drop;
+  debug_settings(&timeout, &drop);
+  const float sl2 = scale * 1.4426950408889634f;
+  const size_t rows = static_cast<size_t>(BH) * Nq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = ws_o + static_cast<size_t>(num_splits) * rows * D;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (D == 64)
-    return causal ? launch<64, true, 4, true, kEmu64>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop)
-                  : launch<64, false, 4, true, kEmu64>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop);
-  return causal ? launch<128, true, 2, false, kEmu128>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop)
-                : launch<128, false, 2, false, kEmu128>(mq, mk, mv, o, lse, BH, Nq, Nk, sl2, st, timeout, drop);
+  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st,
+                                   timeout, drop);
+  if (r != ATTN_OK) return r;
+  return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
+                 : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
 }
 
 const char* attn_strerror(int code) {

@@ -189,8 +189,8 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w):
-    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
+def config_of(w, splits=0):
+    return {"workload": w.name, "split_kv_shares": splits, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
             "causal": w.causal, "scale": w.scale, "sigma_qk": w.sigma_qk, "sigma_v": w.sigma_v,
             "seed": w.seed,
             "l2": ("inputs larger than L2 (%.0f MB > 129 MB); no flush" % (algorithmic_bytes(w) / 1e6))
@@ -205,16 +205,24 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--shape", default=None,
-                    help="B,H,N,D,causal: a custom N(0,1) workload instead of --workload "
-                         "(used for small profiling captures)")
+                    help="B,H,N,D,causal or B,H,Nq,Nk,D,causal: a custom N(0,1) workload "
+                         "instead of --workload (small profiling captures, decode shapes)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="time the split-KV forward with this many key shares (-1: the "
+                         "library's suggestion; 0: the single-pass forward)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.shape:
-        B, H, N, D, c = (int(x) for x in args.shape.split(","))
-        w = synth.Workload(f"custom_{B}x{H}x{N}x{D}{'_causal' if c else ''}", B, H, N, N, D,
-                           bool(c), 1.0, 1.0, 42)
+        vals = [int(x) for x in args.shape.split(",")]
+        if len(vals) == 5:
+            B, H, N, D, c = vals
+            Nq = Nk = N
+        else:
+            B, H, Nq, Nk, D, c = vals
+        name = f"custom_{B}x{H}x{Nq}x{D}" if Nq == Nk else f"custom_{B}x{H}x{Nq}x{Nk}x{D}"
+        w = synth.Workload(name + ("_causal" if c else ""), B, H, Nq, Nk, D, bool(c), 1.0, 1.0, 42)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -248,13 +256,31 @@ def main():
     if algorithmic_bytes(w) <= L2_BYTES:
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
+    splits = args.splits
+    if splits < 0:
+        splits = max(1, attn.splitkv_suggest(w.B, w.H, w.Nq, w.Nk, w.D, w.causal))
+    ws = None
+    if splits > 0:  # workspace allocated once, outside every timed region
+        ws_bytes = attn.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.D, splits)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if splits > 0 else 1
+
+    def call():
+        """One forward through the C ABI on the launching stream."""
+        if splits > 0:
+            code = attn.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal,
+                                         splits, ws.data_ptr(), ws.numel(), sptr)
+        else:
+            code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
+        if code != attn.ATTN_OK:
+            raise attn.AttnError(code, "attn_fwd")
+
     def step():
         if flush is not None:
             flush.fill_(1)
-        code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                             w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
-        if code != attn.ATTN_OK:
-            raise attn.AttnError(code, "attn_fwd")
+        call()
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -278,11 +304,8 @@ def main():
             if flush is not None:
                 flush.fill_(1)
             ev[s][0].record(stream)
-            code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                 w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
+            call()
             ev[s][1].record(stream)
-            if code != attn.ATTN_OK:
-                raise attn.AttnError(code, "attn_fwd")
         t_end.record(stream)
         barrier()
     status = attn.get_status(sptr)
@@ -310,10 +333,7 @@ def main():
             q.copy_(hq, non_blocking=True)
             k.copy_(hk, non_blocking=True)
             v.copy_(hv, non_blocking=True)
-            code = attn.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                 w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, sptr)
-            if code != attn.ATTN_OK:
-                raise attn.AttnError(code, "attn_fwd")
+            call()
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -377,8 +397,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
         "pct_of_peak": 100.0 * value / world / peak,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic", "config": config_of(w), "parallelism": f"replicas x{world} (independent problems)",
-        "gpu_launches": args.steps, "roofline": roofline, "clocks": clk.summary(),
+        "data": "synthetic", "config": config_of(w, splits), "parallelism": f"replicas x{world} (independent problems)",
+        "gpu_launches": args.steps * launches_per_step, "roofline": roofline, "clocks": clk.summary(),
         "e2e": e2e, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

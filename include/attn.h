@@ -31,11 +31,13 @@
 #ifndef ATTN_H
 #define ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define ATTN_VERSION 1
+#define ATTN_VERSION 2
 
 enum {
   ATTN_OK = 0,
@@ -67,6 +69,44 @@ enum {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
              int Nk, int D, float scale, int causal, void* stream);
+
+/*
+ * attn_fwd_splitkv -- the same forward, with the keys of every query tile
+ * divided into num_splits contiguous shares that separate CTAs compute in
+ * parallel, followed by a merge.  This is the split-KV / Flash-Decoding
+ * form the page names in "Relationship to FA-3 and FA-4" ("the monoid's
+ * split-K"): each share yields a partial carrier (its normalised output and
+ * log-sum-exp), and a second kernel combines the shares with the carrier
+ * merge  (m1,d1,o1) (+) (m2,d2,o2) = (m, d1 e^(m1-m) + d2 e^(m2-m),
+ * o1 e^(m1-m) + o2 e^(m2-m)),  m = max(m1, m2).  It pays off when
+ * B*H*ceil(Nq/256) is small next to the SM count (decoding against a long key
+ * sequence); results equal attn_fwd's within rounding.
+ *
+ *   q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, stream: as attn_fwd.
+ *   num_splits  1 .. 256 shares (attn_splitkv_suggest gives one); shares
+ *               that hold no admissible key are allowed.
+ *   workspace   device memory owned by the caller, 16-byte aligned, at least
+ *               attn_splitkv_workspace_bytes(B, H, Nq, D, num_splits) bytes,
+ *               not overlapping any tensor argument.  Its contents on entry
+ *               do not matter; it is overwritten.  Two calls that use the
+ *               same workspace must not run concurrently on the GPU.
+ *
+ * Enqueues two kernels on `stream`.  Errors as attn_fwd, plus ATTN_EINVAL for
+ * num_splits outside 1..256 or a missing / too small workspace and
+ * ATTN_EUNSUPPORTED for a misaligned or overlapping workspace.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int Nq, int Nk, int D, float scale, int causal, int num_splits, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_fwd_splitkv needs: num_splits*B*H*Nq*(D+1)*4.
+ * 0 for negative sizes, D not in {64,128} or num_splits outside 1..256. */
+size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
+
+/* A share count for the current device: enough CTAs to fill its SMs once,
+ * with at least four 128-key tiles per share.  Returns >= 1, or 0 for bad
+ * arguments or when the current device is not supported. */
+int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal);
 
 /* Human-readable text for an ATTN_* code.  Never NULL. */
 const char* attn_strerror(int code);

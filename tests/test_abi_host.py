@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert attn.version() == 1
+    assert attn.version() == 2
     for code in (attn.ATTN_OK, attn.ATTN_EINVAL, attn.ATTN_EUNSUPPORTED, attn.ATTN_ECUDA,
                  attn.ATTN_ETIMEOUT, 99):
         assert isinstance(attn.strerror(code), str) and attn.strerror(code)
@@ -85,3 +85,26 @@ def test_missing_library_fails_loudly(tmp_path):
             _binding.load_library(str(tmp_path / "nope.so"))
     finally:
         _binding._lib = saved
+
+
+def test_splitkv_workspace_bytes(lib):
+    assert attn.splitkv_workspace_bytes(2, 3, 100, 128, 4) == 4 * 2 * 3 * 100 * 129 * 4
+    assert attn.splitkv_workspace_bytes(1, 1, 1, 64, 1) == 65 * 4
+    for bad in [(1, 1, 1, 96, 2), (1, 1, 1, 64, 0), (1, 1, 1, 64, 257), (-1, 1, 1, 64, 2)]:
+        assert attn.splitkv_workspace_bytes(*bad) == 0
+    assert attn.splitkv_suggest(1, 1, 1, 1, 96, 0) == 0
+
+
+W = 1 << 24  # fake 16-byte aligned workspace address, far from A
+
+
+@pytest.mark.parametrize("splits,ws,nbytes,code", [
+    (0, W, 1 << 20, attn.ATTN_EINVAL),           # too few shares
+    (257, W, 1 << 20, attn.ATTN_EINVAL),         # too many shares
+    (2, 0, 1 << 20, attn.ATTN_EINVAL),           # no workspace
+    (2, W, 100, attn.ATTN_EINVAL),               # workspace too small
+    (2, W + 4, 1 << 20, attn.ATTN_EUNSUPPORTED),  # misaligned workspace
+    (2, A, 1 << 20, attn.ATTN_EUNSUPPORTED),     # workspace overlaps q
+])
+def test_splitkv_validation_without_device(lib, splits, ws, nbytes, code):
+    assert attn.attn_fwd_splitkv(A, A, A, 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, splits, ws, nbytes, None) == code
