@@ -13,10 +13,12 @@ import threading
 
 from ._build import LIB_PATH
 
-ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = 0, 1, 2, 3, 4
+ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_ESCRATCH = 0, 1, 2, 3, 4, 5
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 # Every symbol the C header declares; the CPU tests check they are exported.
 EXPORTS = ("attn_fwd", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
+           "attn_fwd_splitkv_noalloc",
            "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
 
 _lock = threading.Lock()
@@ -46,6 +48,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd_splitkv.restype = i32
             lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, i32, vp, ctypes.c_size_t, vp]
+            lib.attn_fwd_splitkv_noalloc.restype = i32
+            lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                     ctypes.c_float, i32, i32, vp]
             lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.attn_splitkv_suggest.restype = i32
@@ -82,6 +87,16 @@ def attn_fwd_splitkv(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: in
     return load_library().attn_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq),
                                            int(Nk), int(D), float(scale), int(bool(causal)),
                                            int(num_splits), ws_ptr, int(ws_bytes), stream)
+
+
+def attn_fwd_splitkv_noalloc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None,
+                             B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+                             num_splits: int, stream: int | None) -> int:
+    """Split-KV forward that allocates nothing: its scratch is a buffer built
+    into the library (see attn.h for the limit and the sharing rules)."""
+    return load_library().attn_fwd_splitkv_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
+                                                   int(Nq), int(Nk), int(D), float(scale),
+                                                   int(bool(causal)), int(num_splits), stream)
 
 
 def splitkv_workspace_bytes(B: int, H: int, Nq: int, D: int, num_splits: int) -> int:

@@ -737,6 +737,27 @@ int launch_merge(const float* ws_o, const float* ws_l, void* o, float* lse, size
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
+// Built-in scratch of attn_fwd_splitkv_noalloc: holds the split-KV parts for
+// callers that cannot allocate device memory.  Every device that loads the
+// library carries it until the process exits.  In host code the name below
+// only stands in for the buffer; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+void* noalloc_scratch_address(int dev) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+    g_noalloc_addr[dev] = ptr;
+  }
+  return g_noalloc_addr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -814,6 +835,39 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                  : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
 }
 
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int Nq, int Nk, int D, float scale, int causal, int num_splits, void* stream) {
+  bool empty = false;
+  const int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_EINVAL;
+  if (empty) return ATTN_OK;
+  if (splitkv_bytes(B, H, Nq, D, num_splits) > kNoAllocScratchBytes) return ATTN_ESCRATCH;
+  const int sms = device_sms();
+  if (sms <= 0) return -sms;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  void* scratch = noalloc_scratch_address(dev);
+  if (scratch == nullptr) return ATTN_ECUDA;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
+    return ATTN_ECUDA;
+  uint64_t timeout;
+  int drop;
+  debug_settings(&timeout, &drop);
+  const float sl2 = scale * 1.4426950408889634f;
+  const size_t rows = static_cast<size_t>(BH) * Nq;
+  float* ws_o = static_cast<float*>(scratch);
+  float* ws_l = ws_o + static_cast<size_t>(num_splits) * rows * D;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st,
+                                   timeout, drop);
+  if (r != ATTN_OK) return r;
+  return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
+                 : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
+}
+
 const char* attn_strerror(int code) {
   switch (code) {
     case ATTN_OK: return "ok";
@@ -821,6 +875,7 @@ const char* attn_strerror(int code) {
     case ATTN_EUNSUPPORTED: return "unsupported argument or device";
     case ATTN_ECUDA: return "CUDA error";
     case ATTN_ETIMEOUT: return "a kernel wait timed out";
+    case ATTN_ESCRATCH: return "the problem needs more scratch than the library's built-in buffer holds";
     default: return "unknown error code";
   }
 }

@@ -45,8 +45,13 @@ enum {
   ATTN_EUNSUPPORTED = 2,  /* D not in {64,128}, misaligned pointer, overlapping output,
                              B*H > 65535, or a device other than sm_103 */
   ATTN_ECUDA = 3,         /* tensor-map encoding or kernel launch failed */
-  ATTN_ETIMEOUT = 4       /* reported by attn_get_status: a kernel wait ran out */
+  ATTN_ETIMEOUT = 4,      /* reported by attn_get_status: a kernel wait ran out */
+  ATTN_ESCRATCH = 5       /* attn_fwd_splitkv_noalloc: problem larger than the built-in scratch */
 };
+
+/* Size of the device buffer compiled into the library for
+ * attn_fwd_splitkv_noalloc (64 MiB on every device that loads the library). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
 
 /*
  * attn_fwd -- O = softmax(scale * Q K^T) V and LSE, fp16 in/out.
@@ -107,6 +112,35 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits)
  * with at least four 128-key tiles per share.  Returns >= 1, or 0 for bad
  * arguments or when the current device is not supported. */
 int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal);
+
+/*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv for callers that cannot
+ * allocate device memory.  Some callers are not allowed to call cudaMalloc
+ * or to hand out a workspace: a serving loop that must never enter an
+ * allocator once it is running (allocation can stall or fail under memory
+ * pressure), or a plugin whose host framework owns all device memory and
+ * passes in only the tensors.  This entry point takes no workspace; the
+ * shares' partial results go to a fixed scratch buffer built into the
+ * library instead.  (The pages have no counterpart: this is a packaging
+ * choice of this library, not part of the method.)
+ *
+ *   Arguments and results: as attn_fwd_splitkv, without workspace arguments.
+ *   Limit: the problem must fit the buffer,
+ *     num_splits * B * H * Nq * (D + 1) * 4 <= ATTN_NOALLOC_SCRATCH_BYTES,
+ *   else ATTN_ESCRATCH is returned and nothing is enqueued.
+ *   The buffer is held by every device that loads the library, until the
+ *   process exits.  The first call on a device looks up the buffer's device
+ *   address (a runtime query that allocates nothing); make that first call
+ *   before any stream capture.
+ *   Every call uses the same buffer, which keeps the last call's contents;
+ *   nothing in it needs to start at zero (each part is written before it
+ *   is read).  Calls whose kernels overlap on the GPU race on the buffer:
+ *   order them (one stream, or events between streams).
+ *   The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *   library routine.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                             int Nq, int Nk, int D, float scale, int causal, int num_splits, void* stream);
 
 /* Human-readable text for an ATTN_* code.  Never NULL. */
 const char* attn_strerror(int code);

@@ -108,3 +108,14 @@ W = 1 << 24  # fake 16-byte aligned workspace address, far from A
 ])
 def test_splitkv_validation_without_device(lib, splits, ws, nbytes, code):
     assert attn.attn_fwd_splitkv(A, A, A, 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, splits, ws, nbytes, None) == code
+
+
+def test_noalloc_rejects_before_touching_the_device(lib):
+    f = attn.attn_fwd_splitkv_noalloc
+    assert f(A, A, A, 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, 0, None) == attn.ATTN_EINVAL
+    assert f(A, A, A, 2 * A, None, 1, 1, 8, 8, 96, 0.1, 0, 2, None) == attn.ATTN_EUNSUPPORTED
+    # 8 * 64 * 16384 * 129 * 4 bytes of parts: larger than the built-in scratch
+    far = 1 << 40  # an output address far from the fake inputs, so no overlap is reported
+    assert f(A, A, A, far, None, 1, 64, 16384, 4096, 128, 0.1, 0, 8, None) == attn.ATTN_ESCRATCH
+    assert "scratch" in attn.strerror(attn.ATTN_ESCRATCH)
+    assert f(A, A, A, 2 * A, None, 0, 4, 8, 8, 64, 0.1, 0, 2, None) == attn.ATTN_OK  # empty problem
