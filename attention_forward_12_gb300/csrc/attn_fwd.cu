@@ -345,25 +345,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // O_w must hold exactly P_0..P_{j-1} before it is rescaled and before
     // P_j is released; every completion of O_w += P_w V is observed in order
     // (in steady state it completed long ago).  The rescale itself is rare
-    // (lazy) and works in 8-column chunks so that it stays light on registers
-    // while the 128-column score row may still be live.
+    // (lazy), except on sharply peaked rows whose maximum keeps growing.
     auto rescale_o = [&](int j, bool resc, float alpha) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT))) return false;
       tc_fence_after();
       if (__any_sync(0xffffffffu, resc)) {
         const float2 al = make_float2(alpha, alpha);
+        if constexpr (SPLIT_P) {
+          // Rescale runs before the exponentials, with the score row live:
+          // 8-column chunks keep it light on registers.
 #pragma unroll 1
-        for (int c = 0; c < HD / 8; ++c) {
-          uint32_t orr[8];
-          tmem_ld8(tO + c * 8, orr);
-          tmem_ld_wait8(orr);
+          for (int c = 0; c < HD / 8; ++c) {
+            uint32_t orr[8];
+            tmem_ld8(tO + c * 8, orr);
+            tmem_ld_wait8(orr);
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
-            orr[e] = __float_as_uint(v.x);
-            orr[e + 1] = __float_as_uint(v.y);
+            for (int e = 0; e < 8; e += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
+              orr[e] = __float_as_uint(v.x);
+              orr[e + 1] = __float_as_uint(v.y);
+            }
+            tmem_st8(tO + c * 8, orr);
           }
-          tmem_st8(tO + c * 8, orr);
+        } else {
+          // Rescale runs after the exponentials (the score row is dead):
+          // full 32-column chunks, unrolled.
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tO + c * 32, orr);
+            tmem_ld_wait(orr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
+              orr[e] = __float_as_uint(v.x);
+              orr[e + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + c * 32, orr);
+          }
         }
       }
       return true;
