@@ -118,24 +118,28 @@ def test_one_dominant_key():
     _run_and_compare(q, k, v, 1.0 / math.sqrt(D), False, "dominant key")
 
 
-def test_running_max_grows_every_tile():
+@pytest.mark.parametrize("D", [64, 128])
+def test_running_max_grows_every_tile(D):
     """Scores rise along the keys by more than the lazy-rescale threshold per
     tile, so every tile rescales O."""
-    B, H, N, D = 1, 2, 1024, 64
+    B, H, N = 1, 2, 1024
     q = np.full((B, H, N, D), 0.5, np.float16)
     ramp = (np.arange(N, dtype=np.float64) / N * 16.0).astype(np.float16)  # 0 .. 16
     k = np.broadcast_to(ramp[None, None, :, None], (B, H, N, D)).astype(np.float16).copy()
     k += synth.normal_fp16((B, H, N, D), 0.05, 7, 1)
     v = synth.normal_fp16((B, H, N, D), 1.0, 7, 2)
-    # score = 0.5 * D * ramp * scale = 4 * ramp: ~11.5 (log2 units) per 128 keys
+    # score = 0.5 * D * ramp / sqrt(D) = 4 * ramp (D=64) or 5.7 * ramp (D=128):
+    # 11.5 or 16 log2 units per 128 keys
     _run_and_compare(q, k, v, 1.0 / math.sqrt(D), False, "growing max")
     _run_and_compare(q, k, v, 1.0 / math.sqrt(D), True, "growing max causal")
 
 
-def test_large_magnitudes():
-    q, k, v = synth.make_qkv(1, 1, 384, 384, 64, 10, sigma_qk=8.0, sigma_v=30.0)
-    o, lse = run_gpu(q, k, v, 0.125, False)
-    O, L = oracle.attn_full(q, k, v, 0.125, False)
+@pytest.mark.parametrize("D", [64, 128])
+def test_large_magnitudes(D):
+    q, k, v = synth.make_qkv(1, 1, 384, 384, D, 10, sigma_qk=8.0, sigma_v=30.0)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, scale, False)
+    O, L = oracle.attn_full(q, k, v, scale, False)
     # V ~ N(0, 30^2): fp16 output rounding scales with |O|, so compare O
     # relative to the scale of V (the absolute bound applies to unit-scale V).
     compare(o.astype(np.float64) / 30.0, lse, O / 30.0, L, "large magnitudes")
@@ -184,3 +188,64 @@ def test_argument_errors_on_device():
     assert f(p, p, p, o.data_ptr(), None, 1, 1, 64, 64, 64, -1.0, False, None) == attn.ATTN_EINVAL
     torch.cuda.synchronize()
     assert attn.get_status() == attn.ATTN_OK
+
+
+# ------------------------------------------------------------ maximum sizes
+
+def test_max_heads_grid_limit():
+    """B*H = 65535, the largest head count the grid takes: every (b, h) is its
+    own problem; compared in full (one query row, three keys each)."""
+    B, H, Nq, Nk, D = 3, 21845, 1, 3, 64
+    q, k, v = synth.make_qkv(B, H, Nq, Nk, D, seed=41)
+    o, lse = run_gpu(q, k, v, 0.125, False)
+    O, L = oracle.attn_full(q, k, v, 0.125, False)
+    compare(o, lse, O, L, "B*H = 65535")
+
+
+@pytest.mark.parametrize("Nk", [1 << 16, 1 << 18])
+def test_long_key_ranges(Nk):
+    """Up to 2^18 keys for a few query rows: 2048 key tiles in one CTA's loop."""
+    B, H, Nq, D = 1, 1, 3, 64
+    q, k, v = synth.make_qkv(B, H, Nq, Nk, D, seed=42, sigma_qk=2.0)
+    o, lse = run_gpu(q, k, v, 0.125, False)
+    O, L = oracle.attn_full(q, k, v, 0.125, False)
+    compare(o, lse, O, L, f"Nk = {Nk}")
+
+
+def test_million_keys_through_split_kv():
+    """2^20 keys: beyond ~2^19 keys the single pass's fp32 tensor-core
+    accumulation of O drifts past the relative-RMS bound, so key ranges this
+    long go through split-KV (16 shares of 2^16 keys, merged in fp32)."""
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    B, H, Nq, Nk, D = 1, 1, 3, 1 << 20, 64
+    qn, kn, vn = synth.make_qkv(B, H, Nq, Nk, D, seed=42, sigma_qk=2.0)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (qn, kn, vn))
+    o, lse = attn.fwd_splitkv(q, k, v, scale=0.125, num_splits=16)
+    torch.cuda.synchronize()
+    assert attn.get_status() == attn.ATTN_OK
+    O, L = oracle.attn_full(qn, kn, vn, 0.125, False)
+    compare(o.cpu().numpy(), lse.cpu().numpy(), O, L, "Nk = 2^20, split-KV x16")
+
+
+def test_over_65535_is_rejected_before_launch():
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    q = torch.zeros(1, 65536, 1, 64, dtype=torch.float16, device="cuda")
+    o = torch.empty_like(q)
+    rc = attn.attn_fwd(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), None, 1, 65536, 1, 1, 64,
+                       0.125, False, None)
+    assert rc == attn.ATTN_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_huge_jump_of_the_running_max(causal):
+    """Scores jump by ~130 log2 units after the first 200 keys: exponentials
+    taken against the old reference would overflow, so the row update must
+    redo the tile against the new one."""
+    B, H, N, D = 1, 2, 640, 128
+    q = np.full((B, H, N, D), 1.0, np.float16)
+    k = synth.normal_fp16((B, H, N, D), 0.05, 8, 1)
+    k[:, :, 200:] += np.float16(8.0)
+    v = synth.normal_fp16((B, H, N, D), 1.0, 8, 2)
+    _run_and_compare(q, k, v, 1.0 / math.sqrt(D), causal, "huge jump")
