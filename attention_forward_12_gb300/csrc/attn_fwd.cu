@@ -20,7 +20,7 @@
 //     each stage guarded by full/empty mbarriers ("New Hardware: TMA": box
 //     copies, hardware swizzle, one issuing thread, mbarrier transaction
 //     counts; "Move 3 -- Pipelining": prefetch under compute).
-//   * MMA issuer (warp 9, one thread): S_w = Q_w K_j^T with tcgen05.mma
+//   * MMA issuer (warp 9; lane 0 issues): S_w = Q_w K_j^T with tcgen05.mma
 //     (A and B from shared memory) into TMEM buffer w, and O_w += P_w V_j
 //     with tcgen05.mma taking P_w from TMEM, where the softmax wrote it over
 //     S_w (the analogue of the page's C->A register repack: P never goes
@@ -260,71 +260,81 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_f16_f32(kBlockM, kBlockN, false, false);
-      constexpr uint32_t kIdescPV = idesc_f16_f32(kBlockM, HD, false, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      // S_w = Q_w K^T of stage s: both operands K-major, 128B swizzle; the
-      // reduction over D runs in steps of 16 (32 bytes inside a swizzle row).
-      auto issue_s = [&](int w, int s) {
-        const uint32_t dS = tmem + w * 128;
+    // The whole warp runs the issue loop, so that every address and
+    // descriptor in it is warp-uniform; lane 0 alone issues (the *_warp
+    // forms).  Descriptors are built once and stepped by adding byte
+    // offsets / 16 to their start-address field (no carry: shared-memory
+    // addresses / 16 fit in its 14 bits).  The base address goes through an
+    // opaque move so that the descriptors are built here, not hoisted above
+    // the role branch where they would hold registers in the softmax warps.
+    uint32_t base;
+    asm volatile("mov.u32 %0, %1;" : "=r"(base) : "r"(smem_u32(sQ)));
+    constexpr uint32_t kIdescQK = idesc_f16_f32(kBlockM, kBlockN, false, false);
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kBlockM, HD, false, true);
+    const uint64_t dQ = smem_desc(base, 16, 1024);
+    const uint64_t dK = smem_desc(base + 2 * TB, 16, 1024);
+    const uint64_t dV = smem_desc(base + (2 + NS) * TB, kChunkBytes, 1024);
+    // S_w = Q_w K^T of stage s: both operands K-major, 128B swizzle; the
+    // reduction over D runs in steps of 16 (32 bytes inside a swizzle row).
+    auto issue_s = [&](int w, int s) {
+      const uint32_t dS = tmem + w * 128;
+      const uint64_t a = dQ + ((w * TB) >> 4);
+      const uint64_t b = dK + ((s * TB) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(dS, smem_desc(aQ + w * TB + off, 16, 1024), smem_desc(aK + s * TB + off, 16, 1024), kIdescQK,
-                  kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[w]);
-      };
-      // O_w += P_w V of stage s: P (fp16, two per column) from TMEM as the A
-      // operand; V MN-major in shared memory (rows = keys, 128 bytes of D per
-      // row; LBO = next 64 columns of D, SBO = next 8 keys).  The first 64 keys
-      // go as soon as the softmax has released the first half of P, so the
-      // tensor core works while the second half is being computed.
-      auto issue_pv = [&](int w, int j, int s) -> bool {
-        const uint32_t aP = tmem + w * 128;
-        const uint32_t dO = tmem + 256 + w * 128;
-        constexpr int kParts = SPLIT_P ? 2 : 1;
-#pragma unroll
-        for (int part = 0; part < kParts; ++part) {
-          const bool last = part == kParts - 1;
-          if (!mbar_wait(last ? &p_full[w] : &p_half[w], j & 1, wc, ATTN_ETIMEOUT)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = part * 8 / kParts; kk < (part + 1) * 8 / kParts; ++kk)
-            umma_ts(dO, aP + kk * 8, smem_desc(aV + s * TB + kk * 2048, kChunkBytes, 1024), kIdescPV,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&o_done[w]);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, wc, ATTN_ETIMEOUT) && mbar_wait(&k_full[0], 0, wc, ATTN_ETIMEOUT);
-      if (ok) {
-        tc_fence_after();
-        if (nkv0 > 0) issue_s(0, 0);
-        if (nkv1 > 0) issue_s(1, 0);
-        umma_commit(&k_empty[0]);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        umma_ss_warp(dS, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
       }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int s = j % NS;
-        const int s1 = (j + 1) % NS;
-        const bool more = j + 1 < nkv;
-        ok = mbar_wait(&v_full[s], (j / NS) & 1, wc, ATTN_ETIMEOUT);
-        if (!ok) break;
+      umma_commit_warp(&s_full[w]);
+    };
+    // O_w += P_w V of stage s: P (fp16, two per column) from TMEM as the A
+    // operand; V MN-major in shared memory (rows = keys, 128 bytes of D per
+    // row; LBO = next 64 columns of D, SBO = next 8 keys).  The first 64 keys
+    // go as soon as the softmax has released the first half of P, so the
+    // tensor core works while the second half is being computed.
+    auto issue_pv = [&](int w, int j, int s) -> bool {
+      const uint32_t aP = tmem + w * 128;
+      const uint32_t dO = tmem + 256 + w * 128;
+      const uint64_t b = dV + ((s * TB) >> 4);
+      constexpr int kParts = SPLIT_P ? 2 : 1;
+#pragma unroll
+      for (int part = 0; part < kParts; ++part) {
+        const bool last = part == kParts - 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(last ? &p_full[w] : &p_half[w], j & 1, wc, ATTN_ETIMEOUT))) return false;
         tc_fence_after();
-        if (j < nkv0 && !(ok = issue_pv(0, j, s))) break;
-        if (more) {
-          ok = mbar_wait(&k_full[s1], ((j + 1) / NS) & 1, wc, ATTN_ETIMEOUT);
-          if (!ok) break;
-          tc_fence_after();
-          if (j + 1 < nkv0) issue_s(0, s1);
-        }
-        if (j < nkv1 && !(ok = issue_pv(1, j, s))) break;
-        umma_commit(&v_empty[s]);
-        if (more) {
-          if (j + 1 < nkv1) issue_s(1, s1);
-          umma_commit(&k_empty[s1]);
-        }
+#pragma unroll
+        for (int kk = part * 8 / kParts; kk < (part + 1) * 8 / kParts; ++kk)
+          umma_ts_warp(dO, aP + kk * 8, b + ((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit_warp(&o_done[w]);
+      return true;
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar, parity, wc, ATTN_ETIMEOUT))) return false;
+      tc_fence_after();
+      return true;
+    };
+    bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+    if (ok) {
+      if (nkv0 > 0) issue_s(0, 0);
+      if (nkv1 > 0) issue_s(1, 0);
+      umma_commit_warp(&k_empty[0]);
+    }
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int s = j % NS;
+      const int s1 = (j + 1) % NS;
+      const bool more = j + 1 < nkv;
+      if (!(ok = wait_all(&v_full[s], (j / NS) & 1))) break;
+      if (j < nkv0 && !(ok = issue_pv(0, j, s))) break;
+      if (more) {
+        if (!(ok = wait_all(&k_full[s1], ((j + 1) / NS) & 1))) break;
+        if (j + 1 < nkv0) issue_s(0, s1);
+      }
+      if (j < nkv1 && !(ok = issue_pv(1, j, s))) break;
+      umma_commit_warp(&v_empty[s]);
+      if (more) {
+        if (j + 1 < nkv1) issue_s(1, s1);
+        umma_commit_warp(&k_empty[s1]);
       }
     }
     __syncwarp();
@@ -550,9 +560,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / NS) & 1, wc, ATTN_ETIMEOUT, false);
       }
     }
-    if (warp == kMmaWarp && lane == 0) {
-      umma_commit(drain);
+    if (warp == kMmaWarp) {
+      umma_commit_warp(drain);
       mbar_wait(drain, 0, wc, ATTN_ETIMEOUT, false);
+      __syncwarp();
     }
     tc_fence_before();
     __syncthreads();

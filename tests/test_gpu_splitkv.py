@@ -42,6 +42,9 @@ CASES = [
     (1, 3, 200, 1000, 64, False, 1),      # one share
     (1, 2, 128, 512, 128, False, 9),      # more shares than key tiles: empty shares
     (2, 2, 700, 900, 64, True, 5),
+    # one key tile per share, the diagonal tile alone in the last one
+    (1, 1, 256, 256, 64, True, 4),
+    (1, 2, 256, 256, 128, True, 4),
 ]
 
 
