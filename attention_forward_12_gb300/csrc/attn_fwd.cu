@@ -110,6 +110,57 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// p = 2^(s*sl2 - m_ref) for one 128-column score row (sr, TMEM columns
+// tS .. tS + 127), packed to fp16 pairs and written back over S in two halves
+// of 64 keys; with SPLIT_P each half is released to the MMA thread as soon
+// as it is in TMEM.  Returns the row sum of the fp32 p.  MASK: 0 = columns
+// >= lim masked when `masked` (decided at run time), 1 = none masked, 2 =
+// columns >= lim masked.
+template <int MASK, int EMU, bool SPLIT_P>
+__device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2v, float2 nm, bool masked, int lim,
+                                         uint32_t tS, uint64_t* p_half, uint64_t* p_full) {
+  const bool mk = MASK == 2 || (MASK == 0 && masked);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * h + cc;
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float2 x =
+            __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl2v, nm);
+        float p0, p1;
+        if (EMU > 0 && (e >> 1) % (EMU > 0 ? EMU : 1) == (EMU > 0 ? EMU : 1) - 1) {
+          const float2 pp = exp2_poly2(x);  // one pair in EMU on the FMA pipe
+          p0 = pp.x;
+          p1 = pp.y;
+        } else {
+          p0 = ex2_approx(x.x);
+          p1 = ex2_approx(x.y);
+        }
+        if (MASK != 1 && mk) {  // -inf * 0 is NaN when scale == 0: select explicitly
+          p0 = (c * 32 + e < lim) ? p0 : 0.f;
+          p1 = (c * 32 + e + 1 < lim) ? p1 : 0.f;
+        }
+        acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], make_float2(p0, p1));
+        pk[cc * 16 + (e >> 1)] = pack_half2(p0, p1);
+      }
+    }
+    tmem_st32(tS + h * 32, pk);
+    if constexpr (SPLIT_P) {
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(h ? p_full : p_half);
+    }
+  }
+  const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 a = __fadd2_rn(a01, a23);
+  return a.x + a.y;
+}
+
 }  // namespace
 
 // Device status word: 0 = ok, otherwise the first ATTN_E* code a kernel
@@ -441,49 +492,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const float2 nm = make_float2(neg_m, neg_m);
 
-      // p = 2^(s*sl2 - m_ref); P goes back over S as fp16 pairs, in two
-      // halves of 64 keys, each released to the MMA thread as soon as it is
-      // in TMEM.
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * h + cc;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
-                                        sl2v, nm);
-            float p0, p1;
-            if (EMU > 0 && (e >> 1) % (EMU > 0 ? EMU : 1) == (EMU > 0 ? EMU : 1) - 1) {
-              const float2 pp = exp2_poly2(x);  // one pair in EMU on the FMA pipe
-              p0 = pp.x;
-              p1 = pp.y;
-            } else {
-              p0 = ex2_approx(x.x);
-              p1 = ex2_approx(x.y);
-            }
-            if (masked) {  // -inf * 0 is NaN when scale == 0: select explicitly
-              p0 = (c * 32 + e < lim) ? p0 : 0.f;
-              p1 = (c * 32 + e + 1 < lim) ? p1 : 0.f;
-            }
-            acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], make_float2(p0, p1));
-            pk[cc * 16 + (e >> 1)] = pack_half2(p0, p1);
-          }
-        }
-        tmem_st32(tS + h * 32, pk);
-        if constexpr (SPLIT_P) {
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(h ? &p_full[wg] : &p_half[wg]);
-        }
+      // p = 2^(s*sl2 - m_ref), written back over S as fp16 pairs (exp_row).
+      // Masked and unmasked tiles run separate copies of the loop where that
+      // was measured to pay (causal, D = 64); the non-causal D = 128 kernel
+      // keeps one loop with the mask decided at run time.
+      if constexpr (CAUSAL || HD == 64) {
+        dsum += masked ? exp_row<2, EMU, SPLIT_P>(sr, sl2v, nm, true, lim, tS, &p_half[wg], &p_full[wg])
+                       : exp_row<1, EMU, SPLIT_P>(sr, sl2v, nm, false, lim, tS, &p_half[wg], &p_full[wg]);
+      } else {
+        dsum += exp_row<0, EMU, SPLIT_P>(sr, sl2v, nm, masked, lim, tS, &p_half[wg], &p_full[wg]);
       }
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a = __fadd2_rn(a01, a23);
-      dsum += a.x + a.y;
       if constexpr (!SPLIT_P) {
         if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
         tmem_st_wait();
