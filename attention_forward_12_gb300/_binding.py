@@ -18,7 +18,7 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 # Every symbol the C header declares; the CPU tests check they are exported.
 EXPORTS = ("attn_fwd", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
-           "attn_fwd_splitkv_noalloc",
+           "attn_fwd_splitkv_noalloc", "attn_fwd_fp8", "attn_fp8_workspace_bytes", "attn_debug_pack_e4m3",
            "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
 
 _lock = threading.Lock()
@@ -51,6 +51,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd_splitkv_noalloc.restype = i32
             lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                      ctypes.c_float, i32, i32, vp]
+            f32 = ctypes.c_float
+            lib.attn_fwd_fp8.restype = i32
+            lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, f32, f32, f32,
+                                         vp, ctypes.c_size_t, vp]
+            lib.attn_fp8_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            lib.attn_debug_pack_e4m3.restype = i32
+            lib.attn_debug_pack_e4m3.argtypes = [vp, vp, i32, vp]
             lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.attn_splitkv_suggest.restype = i32
@@ -97,6 +105,20 @@ def attn_fwd_splitkv_noalloc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse
     return load_library().attn_fwd_splitkv_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
                                                    int(Nq), int(Nk), int(D), float(scale),
                                                    int(bool(causal)), int(num_splits), stream)
+
+
+def attn_fwd_fp8(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None,
+                 B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+                 q_descale: float, k_descale: float, v_descale: float,
+                 ws_ptr: int | None, ws_bytes: int, stream: int | None) -> int:
+    """Direct call of the E4M3 entry point with raw device pointers."""
+    return load_library().attn_fwd_fp8(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq), int(Nk),
+                                       int(D), float(scale), int(bool(causal)), float(q_descale),
+                                       float(k_descale), float(v_descale), ws_ptr, int(ws_bytes), stream)
+
+
+def fp8_workspace_bytes(B: int, H: int, Nk: int, D: int) -> int:
+    return int(load_library().attn_fp8_workspace_bytes(int(B), int(H), int(Nk), int(D)))
 
 
 def splitkv_workspace_bytes(B: int, H: int, Nq: int, D: int, num_splits: int) -> int:
@@ -177,6 +199,59 @@ def fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, num_s
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd_splitkv")
     return out, lse
+
+
+def fwd_fp8(q, k, v, scale: float | None = None, causal: bool = False, q_descale: float = 1.0,
+            k_descale: float = 1.0, v_descale: float = 1.0, workspace=None, out=None, lse=None,
+            want_lse: bool = True):
+    """Forward on E4M3 inputs (see attn.h); returns (o, lse), o fp16.
+
+    q, k, v: contiguous CUDA tensors [B,H,N,128] of one byte per element
+    (torch.float8_e4m3fn, or uint8 holding E4M3 bit patterns).  The
+    workspace (V transposed) is allocated with torch when not given."""
+    import torch
+    byte_types = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype in byte_types):
+            raise TypeError(f"{name} must be a CUDA float8_e4m3fn (or uint8) tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D [B,H,N,D] tensor")
+    B, H, Nq, D = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError("k and v must be [B,H,Nk,D] with q's B, H and D")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    need = fp8_workspace_bytes(B, H, Nk, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, H, Nq, D), dtype=torch.float16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    code = attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, D, scale, causal,
+                        q_descale, k_descale, v_descale, workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _current_stream_ptr(q.device))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_fp8")
+    return out, lse
+
+
+def debug_pack_e4m3(x):
+    """The FP8 forward's E4M3 rounding of P applied to a float32 CUDA tensor
+    (numel a multiple of 4); returns the E4M3 bytes as a uint8 tensor."""
+    import torch
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous CUDA float32 tensor")
+    if x.numel() % 4:
+        raise ValueError("numel must be a multiple of 4")
+    out = torch.empty(x.numel() // 4, dtype=torch.int32, device=x.device)
+    code = load_library().attn_debug_pack_e4m3(x.data_ptr(), out.data_ptr(), x.numel() // 4,
+                                               _current_stream_ptr(x.device))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_debug_pack_e4m3")
+    return out.view(torch.uint8)
 
 
 def get_status(stream: int | None = None) -> int:

@@ -83,10 +83,12 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kEmu64 = 0;
 constexpr int kEmu128 = 0;
 
-template <int HD, int NS>
+template <int HD, int NS, bool FP8 = false>
 struct Layout {
-  static constexpr int kChunks = HD / 64;
-  static constexpr uint32_t kTileBytes = kBlockM * HD * 2;  // one Q, K or V tile
+  static constexpr int kElem = FP8 ? 1 : 2;                   // bytes per element
+  static constexpr int kChunks = HD * kElem / 128;            // 128-byte column blocks per row
+  static constexpr int kChunkElems = 128 / kElem;
+  static constexpr uint32_t kTileBytes = kBlockM * HD * kElem;  // one Q, K or V tile
   static constexpr int kBars = 1 + 4 * NS + 2 + 2 + 2 + 2 + 1;
   static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
 };
@@ -111,44 +113,56 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // p = 2^(s*sl2 - m_ref) for one 128-column score row (sr, TMEM columns
-// tS .. tS + 127), packed to fp16 pairs and written back over S in two halves
-// of 64 keys; with SPLIT_P each half is released to the MMA thread as soon
-// as it is in TMEM.  Returns the row sum of the fp32 p.  MASK: 0 = columns
+// tS .. tS + 127), packed to fp16 pairs (FP8: E4M3 quadruples) and written
+// back over S in two halves of 64 keys; with SPLIT_P each half is released
+// to the MMA thread as soon as it is in TMEM.  Returns the row sum of the fp32 p.  MASK: 0 = columns
 // >= lim masked when `masked` (decided at run time), 1 = none masked, 2 =
 // columns >= lim masked.
-template <int MASK, int EMU, bool SPLIT_P>
+template <int MASK, int EMU, bool SPLIT_P, bool FP8>
 __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2v, float2 nm, bool masked, int lim,
                                          uint32_t tS, uint64_t* p_half, uint64_t* p_full) {
   const bool mk = MASK == 2 || (MASK == 0 && masked);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    uint32_t pk[32];
+    uint32_t pk[FP8 ? 16 : 32];
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * h + cc;
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 x =
-            __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl2v, nm);
-        float p0, p1;
-        if (EMU > 0 && (e >> 1) % (EMU > 0 ? EMU : 1) == (EMU > 0 ? EMU : 1) - 1) {
-          const float2 pp = exp2_poly2(x);  // one pair in EMU on the FMA pipe
-          p0 = pp.x;
-          p1 = pp.y;
+      for (int e = 0; e < 32; e += 4) {
+        float p[4];
+#pragma unroll
+        for (int q = 0; q < 4; q += 2) {
+          const float2 x =
+              __ffma2_rn(make_float2(__uint_as_float(sr[c][e + q]), __uint_as_float(sr[c][e + q + 1])), sl2v, nm);
+          if (EMU > 0 && ((e + q) >> 1) % (EMU > 0 ? EMU : 1) == (EMU > 0 ? EMU : 1) - 1) {
+            const float2 pp = exp2_poly2(x);  // one pair in EMU on the FMA pipe
+            p[q] = pp.x;
+            p[q + 1] = pp.y;
+          } else {
+            p[q] = ex2_approx(x.x);
+            p[q + 1] = ex2_approx(x.y);
+          }
+          if (MASK != 1 && mk) {  // -inf * 0 is NaN when scale == 0: select explicitly
+            p[q] = (c * 32 + e + q < lim) ? p[q] : 0.f;
+            p[q + 1] = (c * 32 + e + q + 1 < lim) ? p[q + 1] : 0.f;
+          }
+          acc[((e + q) >> 1) & 3] = __fadd2_rn(acc[((e + q) >> 1) & 3], make_float2(p[q], p[q + 1]));
+        }
+        if constexpr (FP8) {
+          pk[cc * 8 + (e >> 2)] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
         } else {
-          p0 = ex2_approx(x.x);
-          p1 = ex2_approx(x.y);
+          pk[cc * 16 + (e >> 1)] = pack_half2(p[0], p[1]);
+          pk[cc * 16 + (e >> 1) + 1] = pack_half2(p[2], p[3]);
         }
-        if (MASK != 1 && mk) {  // -inf * 0 is NaN when scale == 0: select explicitly
-          p0 = (c * 32 + e < lim) ? p0 : 0.f;
-          p1 = (c * 32 + e + 1 < lim) ? p1 : 0.f;
-        }
-        acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], make_float2(p0, p1));
-        pk[cc * 16 + (e >> 1)] = pack_half2(p0, p1);
       }
     }
-    tmem_st32(tS + h * 32, pk);
+    if constexpr (FP8) {
+      tmem_st16(tS + h * 16, pk);
+    } else {
+      tmem_st32(tS + h * 32, pk);
+    }
     if constexpr (SPLIT_P) {
       tmem_st_wait();
       tc_fence_before();
@@ -167,14 +181,15 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
 // recorded since the last attn_get_status().
 __device__ int g_attn_status;
 
-template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV>
+template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
                 float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_l, int Nq, int Nk,
-                float sl2, uint64_t timeout_ns,
+                float sl2, float o_scale, uint64_t timeout_ns,
                 int drop_tile) {
-  using L = Layout<HD, NS>;
+  static_assert(!FP8 || (HD == 128 && !SPLIT_P), "the E4M3 kernel is built for D = 128 only");
+  using L = Layout<HD, NS, FP8>;
   constexpr uint32_t TB = L::kTileBytes;
 
   extern __shared__ uint8_t smem_raw[];
@@ -278,10 +293,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_map(&tmV);
       mbar_arrive_expect_tx(q_full, (nkv0 > 0 ? TB : 0) + (nkv1 > 0 ? TB : 0));
       if (nkv0 > 0)
-        for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * 64, r0, bh);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * L::kChunkElems, r0, bh);
       if (nkv1 > 0)
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sQ + TB + c * kChunkBytes, &tmQ, q_full, c * 64, r0 + kBlockM, bh);
+          tma_load_3d(sQ + TB + c * kChunkBytes, &tmQ, q_full, c * L::kChunkElems, r0 + kBlockM, bh);
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
         const int s = j % NS;
@@ -291,14 +307,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (j != drop_tile) {  // drop_tile >= 0 only under attn_debug_set
           mbar_arrive_expect_tx(&k_full[s], TB);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(sK + s * TB + c * kChunkBytes, &tmK, &k_full[s], c * 64, (t0 + j) * kBlockN, bh);
+            tma_load_3d(sK + s * TB + c * kChunkBytes, &tmK, &k_full[s], c * L::kChunkElems, (t0 + j) * kBlockN, bh);
           last_k[s] = j;
         }
         if (j >= NS) ok = mbar_wait(&v_empty[s], ph ^ 1, wc, ATTN_ETIMEOUT);
         if (!ok) break;
         mbar_arrive_expect_tx(&v_full[s], TB);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + s * TB + c * kChunkBytes, &tmV, &v_full[s], c * 64, (t0 + j) * kBlockN, bh);
+        if constexpr (FP8) {
+          // V^T tile: 128 rows of D, each 128 keys (bytes) long.
+          tma_load_3d(sV + s * TB, &tmV, &v_full[s], (t0 + j) * kBlockN, 0, bh);
+        } else {
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sV + s * TB + c * kChunkBytes, &tmV, &v_full[s], c * 64, (t0 + j) * kBlockN, bh);
+        }
         last_v[s] = j;
       }
       // Tail: wait until the tensor core has released every stage, so that
@@ -321,10 +342,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint32_t base;
     asm volatile("mov.u32 %0, %1;" : "=r"(base) : "r"(smem_u32(sQ)));
     constexpr uint32_t kIdescQK = idesc_f16_f32(kBlockM, kBlockN, false, false);
-    constexpr uint32_t kIdescPV = idesc_f16_f32(kBlockM, HD, false, true);
+    // fp16: V is MN-major (LBO = next 64 columns of D); E4M3: V^T is
+    // K-major like K.  (With format code 0, the E4M3 descriptor bits are
+    // those of fp16.)
+    constexpr uint32_t kIdescPV = idesc_f16_f32(kBlockM, HD, false, !FP8);
     const uint64_t dQ = smem_desc(base, 16, 1024);
     const uint64_t dK = smem_desc(base + 2 * TB, 16, 1024);
-    const uint64_t dV = smem_desc(base + (2 + NS) * TB, kChunkBytes, 1024);
+    const uint64_t dV = smem_desc(base + (2 + NS) * TB, FP8 ? 16u : kChunkBytes, 1024);
+    constexpr int kQkSteps = HD * L::kElem / 32;       // 32 bytes of D per product
+    constexpr int kPvSteps = kBlockN * L::kElem / 32;  // 32 bytes of keys per product
     // S_w = Q_w K^T of stage s: both operands K-major, 128B swizzle; the
     // reduction over D runs in steps of 16 (32 bytes inside a swizzle row).
     auto issue_s = [&](int w, int s) {
@@ -332,9 +358,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint64_t a = dQ + ((w * TB) >> 4);
       const uint64_t b = dK + ((s * TB) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
+      for (int kk = 0; kk < kQkSteps; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss_warp(dS, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
+        if constexpr (FP8)
+          umma_ss_f8_warp(dS, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
+        else
+          umma_ss_warp(dS, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
       }
       umma_commit_warp(&s_full[w]);
     };
@@ -354,8 +383,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!__all_sync(0xffffffffu, mbar_wait(last ? &p_full[w] : &p_half[w], j & 1, wc, ATTN_ETIMEOUT))) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kk = part * 8 / kParts; kk < (part + 1) * 8 / kParts; ++kk)
-          umma_ts_warp(dO, aP + kk * 8, b + ((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = part * kPvSteps / kParts; kk < (part + 1) * kPvSteps / kParts; ++kk) {
+          // P: 8 TMEM columns (32 bytes of keys) per product.  V: the next
+          // 16 keys (fp16, 16 rows of 128 B) or 32 keys (V^T, 32 bytes in).
+          if constexpr (FP8)
+            umma_ts_f8_warp(dO, aP + kk * 8, b + ((kk * 32) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          else
+            umma_ts_warp(dO, aP + kk * 8, b + ((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       umma_commit_warp(&o_done[w]);
       return true;
@@ -497,10 +532,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // was measured to pay (causal, D = 64); the non-causal D = 128 kernel
       // keeps one loop with the mask decided at run time.
       if constexpr (CAUSAL || HD == 64) {
-        dsum += masked ? exp_row<2, EMU, SPLIT_P>(sr, sl2v, nm, true, lim, tS, &p_half[wg], &p_full[wg])
-                       : exp_row<1, EMU, SPLIT_P>(sr, sl2v, nm, false, lim, tS, &p_half[wg], &p_full[wg]);
+        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8>(sr, sl2v, nm, true, lim, tS, &p_half[wg], &p_full[wg])
+                       : exp_row<1, EMU, SPLIT_P, FP8>(sr, sl2v, nm, false, lim, tS, &p_half[wg], &p_full[wg]);
       } else {
-        dsum += exp_row<0, EMU, SPLIT_P>(sr, sl2v, nm, masked, lim, tS, &p_half[wg], &p_full[wg]);
+        dsum += exp_row<0, EMU, SPLIT_P, FP8>(sr, sl2v, nm, masked, lim, tS, &p_half[wg], &p_full[wg]);
       }
       if constexpr (!SPLIT_P) {
         if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
@@ -513,7 +548,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (ok && my_nkv > 0 && !SPLITKV) {
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
-      const float inv = 1.f / dsum;
+      const float inv = o_scale / dsum;  // o_scale: the E4M3 kernel's V descale, else 1
       const float2 iv = make_float2(inv, inv);
       __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
 #pragma unroll
@@ -642,6 +677,45 @@ attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restric
   if (lse != nullptr && lane == 0) lse[row] = den > 0.f ? (m + log2f(den)) * 0.69314718055994531f : -INFINITY;
 }
 
+// V^T for the E4M3 kernel, whose O += P V takes V K-major (keys contiguous):
+// vt[bh][d][key] = v[bh][key][d] for D = 128, rows of ldk bytes (the key
+// count rounded up to 16; the keys in between are written as zero).  One CTA
+// per 128 keys of one head, staged through shared memory.
+__global__ void __launch_bounds__(256)
+attn_fp8_transpose_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt, int Nk, int ldk) {
+  __shared__ __align__(16) uint8_t tile[128][128 + 16];
+  const size_t bh = blockIdx.y;
+  const int k0 = blockIdx.x * 128;
+  const uint8_t* src = v + bh * static_cast<size_t>(Nk) * 128;
+  for (int c = threadIdx.x; c < 1024; c += blockDim.x) {
+    const int key = c >> 3, part = c & 7;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + key < Nk) val = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(k0 + key) * 128 + part * 16);
+    *reinterpret_cast<uint4*>(&tile[key][part * 16]) = val;
+  }
+  __syncthreads();
+  uint8_t* dst = vt + bh * 128 * static_cast<size_t>(ldk);
+  for (int c = threadIdx.x; c < 1024; c += blockDim.x) {
+    const int d = c >> 3, kp = c & 7;
+    const int key = k0 + kp * 16;
+    if (key >= ldk) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = kp * 16 + 4 * q;
+      w[q] = static_cast<uint32_t>(tile[r][d]) | (static_cast<uint32_t>(tile[r + 1][d]) << 8) |
+             (static_cast<uint32_t>(tile[r + 2][d]) << 16) | (static_cast<uint32_t>(tile[r + 3][d]) << 24);
+    }
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(d) * ldk + key) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// The softmax's E4M3 packing on its own, for tests: out[i] packs in[4i..4i+3].
+__global__ void attn_debug_pack_e4m3_kernel(const float* __restrict__ in, uint32_t* __restrict__ out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = pack_e4m3x4(in[4 * i], in[4 * i + 1], in[4 * i + 2], in[4 * i + 3]);
+}
+
 // =====================================================================
 // Host side
 // =====================================================================
@@ -685,24 +759,39 @@ bool make_map(CUtensorMap* m, const void* base, int64_t BH, int64_t N, int D) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 tensors as bytes: [BH, rows, cols] with row stride ld (a multiple of
+// 16 bytes); box = 128 x 128 x 1 with the 128-byte swizzle.  Elements past
+// cols or rows read as zero.
+bool make_map_u8(CUtensorMap* m, const void* base, int64_t BH, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld), static_cast<cuuint64_t>(rows * ld)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
 }
 
-template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV>
+template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
                float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
-               uint64_t timeout_ns, int drop) {
-  using L = Layout<HD, NS>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV>;
+               uint64_t timeout_ns, int drop, float o_scale = 1.0f) {
+  using L = Layout<HD, NS, FP8>;
+  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
       cudaSuccess)
     return ATTN_ECUDA;
   dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, splits);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         timeout_ns, drop);
+                                         o_scale, timeout_ns, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
@@ -914,6 +1003,68 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
   if (r != ATTN_OK) return r;
   return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
                  : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
+}
+
+size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D) {
+  if (B < 0 || H < 0 || Nk < 0 || D != 128) return 0;
+  return static_cast<size_t>(B) * H * D * ((static_cast<size_t>(Nk) + 15) / 16 * 16);
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int D, float scale, int causal, float q_descale, float k_descale, float v_descale, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o) return ATTN_EINVAL;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return ATTN_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_EINVAL;
+  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale) || q_descale <= 0.f ||
+      k_descale <= 0.f || v_descale <= 0.f)
+    return ATTN_EINVAL;
+  if (D != 128) return ATTN_EUNSUPPORTED;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_EUNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535) return ATTN_EUNSUPPORTED;
+  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
+  const size_t need = attn_fp8_workspace_bytes(B, H, Nk, D);
+  if (!workspace || workspace_bytes < need) return ATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_EUNSUPPORTED;
+  const int BH = B * H;
+  const size_t qb = static_cast<size_t>(BH) * Nq * D, kb = static_cast<size_t>(BH) * Nk * D;
+  const size_t ob = qb * 2, lb = static_cast<size_t>(BH) * Nq * 4;
+  if (ranges_overlap(o, ob, q, qb) || ranges_overlap(o, ob, k, kb) || ranges_overlap(o, ob, v, kb) ||
+      ranges_overlap(workspace, need, q, qb) || ranges_overlap(workspace, need, k, kb) ||
+      ranges_overlap(workspace, need, v, kb) || ranges_overlap(workspace, need, o, ob))
+    return ATTN_EUNSUPPORTED;
+  if (lse && (ranges_overlap(lse, lb, o, ob) || ranges_overlap(lse, lb, q, qb) || ranges_overlap(lse, lb, k, kb) ||
+              ranges_overlap(lse, lb, v, kb) || ranges_overlap(lse, lb, workspace, need)))
+    return ATTN_EUNSUPPORTED;
+  const int sms = device_sms();
+  if (sms <= 0) return -sms;
+  const int ldk = (Nk + 15) / 16 * 16;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_u8(&mq, q, BH, Nq, D, D) || !make_map_u8(&mk, k, BH, Nk, D, D) ||
+      !make_map_u8(&mv, workspace, BH, D, Nk, ldk))
+    return ATTN_ECUDA;
+  uint64_t timeout;
+  int drop;
+  debug_settings(&timeout, &drop);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  attn_fp8_transpose_v_kernel<<<dim3((Nk + 127) / 128, BH), 256, 0, st>>>(static_cast<const uint8_t*>(v),
+                                                                          static_cast<uint8_t*>(workspace), Nk, ldk);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ECUDA;
+  const float sl2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  return causal ? launch_fwd<128, true, 4, false, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
+                                                                  sl2, 1, st, timeout, drop, v_descale)
+                : launch_fwd<128, false, 4, false, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
+                                                                   sl2, 1, st, timeout, drop, v_descale);
+}
+
+int attn_debug_pack_e4m3(const float* in, unsigned int* out, int n_quads, void* stream) {
+  if (!in || !out || n_quads < 0) return ATTN_EINVAL;
+  if (n_quads == 0) return ATTN_OK;
+  attn_debug_pack_e4m3_kernel<<<(n_quads + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      in, reinterpret_cast<uint32_t*>(out), n_quads);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
 const char* attn_strerror(int code) {

@@ -193,6 +193,14 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), ATTN_S8(0), ATTN_S8(8)
+      : "memory");
+}
+
 #undef ATTN_R8
 #undef ATTN_W8
 #undef ATTN_S8
@@ -272,6 +280,33 @@ __device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// The same two products with 8-bit operands (tcgen05.mma.kind::f8f6f4;
+// with A and B format code 0 in the instruction descriptor both are E4M3,
+// and one instruction reduces over 32 elements of K, still 32 bytes).
+__device__ __forceinline__ void umma_ss_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .u32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\t"
+      "setp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_f8_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .u32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\t"
+      "setp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\t"
@@ -293,6 +328,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Four floats rounded to OCP FP8 E4M3 (round to nearest even, saturating
+// to +-448), packed little-endian: a in bits 0-7, b in 8-15, c in 16-23, d
+// in 24-31 -- the order of consecutive elements in memory and in TMEM.
+// cvt.rn.satfinite.e4m3x2.f32 puts its first source in the upper byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 // 2^x for a pair of floats on the FMA pipe instead of the MUFU unit.

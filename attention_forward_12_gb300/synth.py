@@ -102,6 +102,37 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, D: int, seed: int,
     return q, k, v
 
 
+def _e4m3_positive_values() -> np.ndarray:
+    """Magnitudes of the OCP FP8 E4M3 codes 0..126 (ascending): codes below 8
+    are subnormal, c/8 * 2^-6; the others (1 + (c mod 8)/8) * 2^(c div 8 - 7).
+    Code 127 is NaN."""
+    c = np.arange(127)
+    return np.where(c < 8, c / 8.0 * 2.0 ** -6, (1.0 + (c & 7) / 8.0) * 2.0 ** ((c >> 3) - 7))
+
+
+def to_e4m3(x) -> np.ndarray:
+    """E4M3 codes (uint8) nearest to x: round to nearest, ties to the even
+    code, magnitudes above 448 saturate to 448 (as a "satfinite" conversion).
+    Input rounding only -- it serves the generators below."""
+    x = np.asarray(x, dtype=np.float64)
+    vals = _e4m3_positive_values()
+    a = np.minimum(np.abs(x), vals[-1])
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 1, 126)
+    lo = hi - 1
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a == 0, 0, code)
+    return (code | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
+
+
+def make_qkv_e4m3(B: int, H: int, Nq: int, Nk: int, D: int, seed: int,
+                  sigma_qk: float = 1.0, sigma_v: float = 1.0):
+    """(q, k, v) as E4M3 codes (uint8 numpy arrays): the fp16 draws of
+    make_qkv rounded to the nearest E4M3 value."""
+    return tuple(to_e4m3(x.astype(np.float64)) for x in make_qkv(B, H, Nq, Nk, D, seed, sigma_qk, sigma_v))
+
+
 def workload_qkv(w: Workload):
     return make_qkv(w.B, w.H, w.Nq, w.Nk, w.D, w.seed, w.sigma_qk, w.sigma_v)
 

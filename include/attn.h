@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define ATTN_VERSION 2
+#define ATTN_VERSION 3
 
 enum {
   ATTN_OK = 0,
@@ -147,6 +147,54 @@ int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal);
  */
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                              int Nq, int Nk, int D, float scale, int causal, int num_splits, void* stream);
+
+/*
+ * attn_fwd_fp8 -- the forward on 8-bit inputs: Q, K and V in OCP FP8 E4M3
+ * (one byte each; 4 exponent bits, bias 7, 3 mantissa bits, largest finite
+ * value 448), both products on the tensor core's 8-bit path with fp32
+ * accumulation.  This is the lower-precision route the pages point to for
+ * the newer tensor cores ("faster lower-precision tensor cores"; FA-3 and
+ * FA-4's low-precision paths in "Relationship to FA-3 and FA-4"); the pages
+ * give no kernel for it, and this one is the fp16 kernel with 8-bit
+ * operands:
+ *
+ *   S = scale * (q_descale Q)(k_descale K)^T,  p = 2^(S log2 e - m),
+ *   P rounded to E4M3 (round to nearest even; p <= 256 by the lazy rescale,
+ *   inside the format's range), O = v_descale * (P V) / sum p  in fp16,
+ *   LSE as attn_fwd, of the descaled scores.
+ *
+ *   q      [B,H,Nq,128] E4M3 bytes, 16-byte aligned.
+ *   k, v   [B,H,Nk,128] E4M3 bytes, 16-byte aligned.
+ *   o      [B,H,Nq,128] fp16, 16-byte aligned, written; lse as attn_fwd.
+ *   q_descale, k_descale, v_descale  per-tensor factors, finite and > 0,
+ *          that the stored values are multiplied by (1 for unscaled data).
+ *   workspace  device memory owned by the caller, 16-byte aligned, at least
+ *          attn_fp8_workspace_bytes(B, H, Nk, D) bytes, not overlapping any
+ *          tensor: receives V transposed ([B,H,128,Nk] with rows rounded up
+ *          to 16 bytes), which the P V product reads with keys contiguous.
+ *          Two calls that share a workspace must not run concurrently.
+ *   B, H, Nq, Nk, scale, causal, stream: as attn_fwd.  D must be 128.
+ *
+ * Enqueues two kernels (the transpose, then the forward) on `stream`.
+ * Errors as attn_fwd, plus ATTN_EINVAL for a descale that is not finite and
+ * positive or a missing / too small workspace, ATTN_EUNSUPPORTED for D != 128
+ * or a misaligned or overlapping workspace.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                 int Nk, int D, float scale, int causal, float q_descale, float k_descale, float v_descale,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_fwd_fp8 needs: B*H*D*round_up(Nk, 16).  0 for
+ * negative sizes or D != 128. */
+size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D);
+
+/*
+ * Testing hook: the E4M3 rounding the FP8 forward applies to P, on its own.
+ * in: 4*n_quads fp32 values (device); out: n_quads words (device), word i
+ * holding in[4i] in bits 0-7 ... in[4i+3] in bits 24-31.  Asynchronous on
+ * `stream`.  ATTN_EINVAL for null pointers or n_quads < 0.
+ */
+int attn_debug_pack_e4m3(const float* in, unsigned int* out, int n_quads, void* stream);
 
 /* Human-readable text for an ATTN_* code.  Never NULL. */
 const char* attn_strerror(int code);

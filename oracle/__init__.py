@@ -148,6 +148,55 @@ def attn_full(q, k, v, scale: float, causal: bool, nthreads: int = 0):
 
 
 # ---------------------------------------------------------------------------
+# 8-bit inputs: OCP FP8 E4M3.
+# ---------------------------------------------------------------------------
+
+def e4m3_to_double(codes) -> np.ndarray:
+    """Exact value of OCP FP8 E4M3 codes (the "fn" variant of the OCP 8-bit
+    floating point specification: no infinities, S.1111.111 is NaN).  Bit 7
+    is the sign, bits 6-3 the exponent E (bias 7), bits 2-0 the mantissa M:
+    E = 0 gives (-1)^S * M/8 * 2^-6, otherwise (-1)^S * (1 + M/8) * 2^(E-7)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (8 + m) * np.exp2(e - 10.0))
+    return np.where((c & 0x7F) == 0x7F, np.nan, sign * mag)
+
+
+def _e4m3_as_fp16(codes) -> np.ndarray:
+    """E4M3 codes as fp16 arrays: every E4M3 value is an fp16 value (3 of the
+    10 mantissa bits, exponents -9 .. 8), so the conversion is exact."""
+    d = e4m3_to_double(codes)
+    h = d.astype(np.float16)
+    if not np.array_equal(h.astype(np.float64), d, equal_nan=True):
+        raise AssertionError("E4M3 -> fp16 must be exact")
+    return h
+
+
+def attn_rows_e4m3(q8, k8, v8, scale: float, causal: bool, q_descale: float = 1.0,
+                   k_descale: float = 1.0, v_descale: float = 1.0, rows=None, nthreads: int = 0,
+                   want_probs: bool = False):
+    """O and LSE (fp64) on E4M3 inputs: the plain definition over the exact
+    values q_descale*Q, k_descale*K, v_descale*V, i.e. the fp16 oracle on the
+    decoded codes with scale * q_descale * k_descale, and O times v_descale.
+    Returns (O, LSE, threads) or, with want_probs, (O, LSE, P, threads), P
+    the softmax weights [n, Nk]."""
+    q, k, v = (_e4m3_as_fp16(x) for x in (q8, k8, v8))
+    res = attn_rows(q, k, v, float(scale) * float(q_descale) * float(k_descale), causal, rows, nthreads,
+                    want_probs)
+    return (res[0] * float(v_descale),) + tuple(res[1:])
+
+
+def attn_full_e4m3(q8, k8, v8, scale: float, causal: bool, q_descale: float = 1.0,
+                   k_descale: float = 1.0, v_descale: float = 1.0, nthreads: int = 0):
+    """O [B,H,Nq,D] and LSE [B,H,Nq] (fp64) for every row, E4M3 inputs."""
+    B, H, Nq, D = np.asarray(q8).shape
+    o, lse, _ = attn_rows_e4m3(q8, k8, v8, scale, causal, q_descale, k_descale, v_descale, None, nthreads)
+    return o.reshape(B, H, Nq, D), lse.reshape(B, H, Nq)
+
+
+# ---------------------------------------------------------------------------
 # Streaming carrier (m, d, o) -- a second, separately written implementation.
 # ---------------------------------------------------------------------------
 

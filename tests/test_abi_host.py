@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert attn.version() == 2
+    assert attn.version() == 3
     for code in (attn.ATTN_OK, attn.ATTN_EINVAL, attn.ATTN_EUNSUPPORTED, attn.ATTN_ECUDA,
                  attn.ATTN_ETIMEOUT, 99):
         assert isinstance(attn.strerror(code), str) and attn.strerror(code)
@@ -119,3 +119,43 @@ def test_noalloc_rejects_before_touching_the_device(lib):
     assert f(A, A, A, far, None, 1, 64, 16384, 4096, 128, 0.1, 0, 8, None) == attn.ATTN_ESCRATCH
     assert "scratch" in attn.strerror(attn.ATTN_ESCRATCH)
     assert f(A, A, A, 2 * A, None, 0, 4, 8, 8, 64, 0.1, 0, 2, None) == attn.ATTN_OK  # empty problem
+
+
+def test_fp8_workspace_bytes(lib):
+    assert attn.fp8_workspace_bytes(2, 3, 100, 128) == 2 * 3 * 128 * 112  # rows rounded up to 16 keys
+    assert attn.fp8_workspace_bytes(1, 1, 16, 128) == 128 * 16
+    for bad in [(1, 1, 16, 64), (1, 1, 16, 96), (-1, 1, 16, 128)]:
+        assert attn.fp8_workspace_bytes(*bad) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    # q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, qd, kd, vd, ws, ws_bytes
+    ((0, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, W, 1 << 20), attn.ATTN_EINVAL),   # null q
+    ((A, A, A, 2 * A, None, 1, 1, 8, 0, 128, 0.1, 0, 1.0, 1.0, 1.0, W, 1 << 20), attn.ATTN_EINVAL),   # Nk = 0
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 0.0, 1.0, 1.0, W, 1 << 20), attn.ATTN_EINVAL),   # q_descale 0
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, float("inf"), 1.0, W, 1 << 20), attn.ATTN_EINVAL),
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, -2.0, W, 1 << 20), attn.ATTN_EINVAL),  # v_descale < 0
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, 1.0, 1.0, 1.0, W, 1 << 20), attn.ATTN_EUNSUPPORTED),  # D
+    ((A + 8, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, W, 1 << 20), attn.ATTN_EUNSUPPORTED),
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, 0, 1 << 20), attn.ATTN_EINVAL),   # no workspace
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, W, 100), attn.ATTN_EINVAL),      # too small
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, W + 4, 1 << 20), attn.ATTN_EUNSUPPORTED),
+    ((A, A, A, 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, A, 1 << 20), attn.ATTN_EUNSUPPORTED),  # ws on q
+    ((A, A, A, A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, W, 1 << 20), attn.ATTN_EUNSUPPORTED),  # o on q
+    ((A, A, A, 2 * A, None, 0, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0, 0, 0), attn.ATTN_OK),             # empty
+])
+def test_fp8_validation_without_device(lib, args, code):
+    assert attn.attn_fwd_fp8(*args, None) == code
+
+
+def test_fp8_binding_refuses_fp16(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 4, 128, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        attn.fwd_fp8(x, x, x)
+
+
+def test_debug_pack_validation(lib):
+    assert lib.attn_debug_pack_e4m3(None, None, 4, None) == attn.ATTN_EINVAL
+    assert lib.attn_debug_pack_e4m3(A, A, -1, None) == attn.ATTN_EINVAL
+    assert lib.attn_debug_pack_e4m3(A, A, 0, None) == attn.ATTN_OK

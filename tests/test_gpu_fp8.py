@@ -1,0 +1,131 @@
+"""The E4M3 forward (attn_fwd_fp8) against the fp64 oracle evaluated on the
+exactly decoded inputs.
+
+Tolerance, derived from the kernel's arithmetic.  The products are exact
+(E4M3 x E4M3 fits fp32) and accumulated in fp32; what the 8-bit path adds is
+the rounding of P to E4M3 before P V (round to nearest even: relative error
+<= 2^-4 for p >= 2^-6, absolute error <= 2^-10 below), while the row sum d
+takes the unrounded fp32 p.  With w_j the softmax weights, the GPU's p_j is
+w_j d and d >= 1 / max_j w_j (its reference maximum never exceeds the row's
+maximum), so for every element
+
+    |O_gpu - O| <= v_descale (2^-4 sum_j w_j |v_j| + 2^-10 max_j w_j sum_j |v_j|)
+                   + 2^-11 |O| (fp16 output) + 1e-5 v_descale sum_j w_j |v_j| (fp32 sums, scale)
+
+and, the rounding errors being independent with relative RMS 2^-3 / sqrt(12)
+* sqrt(E[1/m^2]) ~= 0.027 over a binade, the relative RMS error of O is
+about 0.027: the tests require <= 0.05.  LSE does not see P's rounding: its
+bound stays 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from attention_forward_12_gb300 import synth
+from gpu_common import torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+TOL_FP8_RELRMS = 0.05
+TOL_FP8_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    torch_cuda()
+    import attention_forward_12_gb300 as attn
+    attn.build()
+    attn.load_library()
+
+
+def run_fp8(q8, k8, v8, scale, causal, qd=1.0, kd=1.0, vd=1.0):
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (q8, k8, v8))
+    o, lse = attn.fwd_fp8(tq, tk, tv, scale=scale, causal=causal, q_descale=qd, k_descale=kd, v_descale=vd)
+    torch.cuda.synchronize()
+    assert attn.get_status() == attn.ATTN_OK
+    return o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def check_fp8(o, lse, q8, k8, v8, scale, causal, qd=1.0, kd=1.0, vd=1.0, rows=None, label=""):
+    B, H, Nq, D = q8.shape
+    Nk = k8.shape[2]
+    O, L, P, _ = oracle.attn_rows_e4m3(q8, k8, v8, scale, causal, qd, kd, vd, rows=rows, want_probs=True)
+    rows = np.arange(B * H * Nq) if rows is None else np.asarray(rows)
+    og = o.reshape(-1, D)[rows]
+    lg = lse.reshape(-1)[rows]
+    assert np.all(np.isfinite(og)) and np.all(np.isfinite(lg)), f"{label}: non-finite output"
+    av = np.abs(oracle.e4m3_to_double(v8)).reshape(B * H, Nk, D)
+    bound = np.empty_like(O)
+    for bh in np.unique(rows // Nq):
+        sel = np.nonzero(rows // Nq == bh)[0]
+        wv = P[sel] @ av[bh]                                   # sum_j w_j |v_j|
+        bound[sel] = vd * ((2.0 ** -4 + 1e-5) * wv + 2.0 ** -10 * P[sel].max(1)[:, None] * av[bh].sum(0))
+    bound += 2.0 ** -11 * np.abs(O)
+    diff = og - O
+    excess = float((np.abs(diff) - bound).max())  # elements with bound 0 (v = 0) must be exact
+    worst = float((np.abs(diff) / np.where(bound > 0, bound, 1.0)).max())
+    rel_rms = float(np.linalg.norm(diff) / np.linalg.norm(O))
+    lse_err = float(np.abs(lg - L).max())
+    assert excess <= 0.0, f"{label}: an element exceeds its rounding bound ({worst:.3f} of it)"
+    assert rel_rms <= TOL_FP8_RELRMS, f"{label}: O rel-RMS {rel_rms:.3e}"
+    assert lse_err <= TOL_FP8_LSE, f"{label}: LSE max-abs {lse_err:.3e}"
+    return worst, rel_rms, lse_err
+
+
+CASES = [
+    # B, H, Nq, Nk, causal, sigma_qk, seed
+    (1, 2, 256, 300, False, 1.0, 1),      # ragged key tail
+    (1, 2, 300, 256, True, 1.0, 2),       # ragged query tail, causal
+    (2, 2, 130, 515, True, 1.0, 3),       # causal with Nq != Nk
+    (1, 1, 5, 3, False, 1.0, 4),          # smaller than a tile
+    (1, 3, 64, 1, True, 1.0, 5),          # one key
+    (1, 2, 1000, 1000, True, 1.0, 6),
+    (1, 4, 512, 4096, False, 3.0, 7),     # peaked rows: the running maximum keeps growing
+    (1, 2, 256, 16384, False, 1.0, 8),    # long key range
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,causal,sqk,seed", CASES)
+def test_fp8_matches_oracle(B, H, Nq, Nk, causal, sqk, seed):
+    q8, k8, v8 = synth.make_qkv_e4m3(B, H, Nq, Nk, 128, seed=4000 + seed, sigma_qk=sqk)
+    o, lse = run_fp8(q8, k8, v8, 128 ** -0.5, causal)
+    check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, causal, label=f"[{B},{H},{Nq},{Nk}] causal={causal}")
+
+
+def test_fp8_descales():
+    q8, k8, v8 = synth.make_qkv_e4m3(1, 2, 256, 2048, 128, seed=4100, sigma_qk=2.0)
+    args = dict(qd=0.5, kd=3.0, vd=0.25)
+    o, lse = run_fp8(q8, k8, v8, 128 ** -0.5, False, **args)
+    check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, False, label="descales", **args)
+
+
+def test_fp8_full_size_peaked_sampled_rows():
+    """The peaked [4,32,16384,128] workload in E4M3, in the single launch the
+    benchmark times, checked on sampled rows."""
+    B, H, N = 4, 32, 16384
+    q8, k8, v8 = synth.make_qkv_e4m3(B, H, N, N, 128, seed=5, sigma_qk=3.0)
+    o, lse = run_fp8(q8, k8, v8, 128 ** -0.5, False)
+    rows = synth.sample_rows(B, H, N, 384, seed=4200, head_rows=128)
+    check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, False, rows=rows, label="peaked E4M3 sampled")
+
+
+def test_pack_e4m3_is_round_to_nearest_even_with_saturation():
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(3)
+    vals = oracle.e4m3_to_double(np.arange(127, dtype=np.uint8))
+    ties = (vals[:-1] + vals[1:]) / 2
+    x = np.concatenate([rng.standard_normal(4000) * s for s in (1e-3, 0.02, 1.0, 30.0, 120.0)]
+                       + [ties, -ties, [0.0, 448.0, 464.0, 470.0, 1e6, -1e6, 3 * 2.0 ** -10]])
+    x = x[: len(x) // 4 * 4].astype(np.float32)
+    got = attn.debug_pack_e4m3(torch.from_numpy(x).cuda()).cpu().numpy()
+    ref = torch.from_numpy(x.astype(np.float64)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    sat = np.abs(x) > 464.0  # satfinite: past the top rounding boundary, +-448
+    ref = np.where(sat, np.where(x > 0, 0x7E, 0xFE), ref).astype(np.uint8)
+    assert np.array_equal(got, ref)
