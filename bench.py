@@ -224,6 +224,8 @@ def main():
     ap.add_argument("--splits", type=int, default=0,
                     help="time the split-KV forward with this many key shares (-1: the "
                          "library's suggestion; 0: the single-pass forward)")
+    ap.add_argument("--dtype", choices=["f16", "e4m3"], default="f16",
+                    help="input precision: fp16 (attn_fwd) or FP8 E4M3 (attn_fwd_fp8, D = 128)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
@@ -257,12 +259,15 @@ def main():
 
     # inputs: seeded on the host (the same bytes the oracle sees), copied once;
     # every rank draws its own independent problems of the workload's shape
-    qn, kn, vn = synth.make_qkv(w.B, w.H, w.Nq, w.Nk, w.D, multirank.rank_seed(w.seed, rank),
-                                w.sigma_qk, w.sigma_v)
+    fp8 = args.dtype == "e4m3"
+    if fp8 and (w.D != 128 or args.splits != 0):
+        raise SystemExit("--dtype e4m3 runs the single-pass forward at D = 128")
+    gen_qkv = synth.make_qkv_e4m3 if fp8 else synth.make_qkv
+    qn, kn, vn = gen_qkv(w.B, w.H, w.Nq, w.Nk, w.D, multirank.rank_seed(w.seed, rank), w.sigma_qk, w.sigma_v)
     q = torch.from_numpy(qn).to(dev)
     k = torch.from_numpy(kn).to(dev)
     v = torch.from_numpy(vn).to(dev)
-    o = torch.empty_like(q)
+    o = torch.empty((w.B, w.H, w.Nq, w.D), dtype=torch.float16, device=dev)
     lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
@@ -277,11 +282,18 @@ def main():
     if splits > 0:  # workspace allocated once, outside every timed region
         ws_bytes = attn.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.D, splits)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    launches_per_step = 2 if splits > 0 else 1
+    if fp8:  # V^T workspace, allocated once outside every timed region
+        ws_bytes = attn.fp8_workspace_bytes(w.B, w.H, w.Nk, w.D)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if (splits > 0 or fp8) else 1
 
     def call():
         """One forward through the C ABI on the launching stream."""
-        if splits > 0:
+        if fp8:
+            code = attn.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, 1.0, 1.0, 1.0,
+                                     ws.data_ptr(), ws.numel(), sptr)
+        elif splits > 0:
             code = attn.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal,
                                          splits, ws.data_ptr(), ws.numel(), sptr)
@@ -340,7 +352,7 @@ def main():
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (qn, kn, vn))
-        ho = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+        ho = torch.empty(o.shape, dtype=torch.float16).pin_memory()
         hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
 
         def e2e_step():
@@ -365,7 +377,8 @@ def main():
         e_ms = multirank.max_over_ranks(e_ms, dist, dev)
         e2e = {"value": multirank.aggregate_tflops(f, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "steps": n_e2e,
-               "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+               "h2d_bytes_per_step": int(hq.numel() * hq.element_size() + hk.numel() * hk.element_size()
+                                         + hv.numel() * hv.element_size()),
                "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4)}
         assert attn.get_status(sptr) == attn.ATTN_OK
 
@@ -381,13 +394,18 @@ def main():
         peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
     else:
         peak = peak_sus = FALLBACK_PEAK_TFLOPS
+    peak_note = f"bf16_tflops (burst) of {peak_src}; fp16 dense = bf16 dense"
+    nominal = 2250.0
+    if fp8:  # no measured fp8 peak: the bf16 one times the nominal dense ratio 4.5 / 2.25
+        peak, peak_sus, nominal = 2.0 * peak, 2.0 * peak_sus, 4500.0
+        peak_note = f"2 x bf16_tflops (burst) of {peak_src}: fp8 dense = 2 x bf16 dense nominally"
     achieved = f / (kern_avg_ms * 1e-3) / 1e12
-    traffic, traffic_note = recorded_traffic(w.name)
+    traffic, traffic_note = recorded_traffic(w.name + ("_e4m3" if fp8 else ""))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"bf16_tflops (burst) of {peak_src}; fp16 dense = bf16 dense",
+                "peak_source": peak_note,
                 "peak_sustained": peak_sus, "frac_sustained": achieved / peak_sus,
-                "frac_of_nominal_2250": achieved / 2250.0,
+                f"frac_of_nominal_{int(nominal)}": achieved / nominal,
                 "kernel_ms_avg": kern_avg_ms, "kernel_ms_min": min(kernel_ms),
                 "algorithmic_flops_per_launch": f}
     if traffic_note:
@@ -395,8 +413,13 @@ def main():
 
     cpu = None
     if world == 1:
-        rows, O, L, el, threads, done = oracle_sample(w, qn, kn, vn, args.cpu_seconds, seed=w.seed)
         import numpy as np
+        if fp8:  # the oracle on the exactly decoded inputs (every E4M3 value is an fp16 value)
+            import oracle
+            qo, ko, vo = (oracle.e4m3_to_double(x).astype(np.float16) for x in (qn, kn, vn))
+        else:
+            qo, ko, vo = qn, kn, vn
+        rows, O, L, el, threads, done = oracle_sample(w, qo, ko, vo, args.cpu_seconds, seed=w.seed)
         og = o.view(-1, w.D)[torch.from_numpy(rows).to(dev)].float().cpu().numpy().astype(np.float64)
         lg = lse.view(-1)[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
         cpu = {"value": done / el / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -410,7 +433,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
         "pct_of_peak": 100.0 * value / world / peak,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
         "data": "synthetic", "config": config_of(w, splits), "parallelism": f"replicas x{world} (independent problems)",
         "gpu_launches": args.steps * launches_per_step, "roofline": roofline, "clocks": clk.summary(),
         "e2e": e2e, "cpu_baseline": cpu,
