@@ -27,16 +27,19 @@
 //     through shared memory).  Issue order per key tile j:
 //         O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
 //     so that one warpgroup's softmax runs while the tensor core works on
-//     the other's tile.  With SPLIT_P (used at D=64, where the row update
-//     outweighs the matmuls) each O_w += P_w V_j is issued in two halves of
-//     64 keys: the first as soon as the softmax has released the first half
-//     of P_w, overlapping the second half's exponentials.
+//     the other's tile.  With SPLIT_P (the fp16 kernels) each O_w += P_w V_j
+//     is issued in two halves of 64 keys: the first as soon as the softmax
+//     has released the first half of P_w, overlapping the second half's
+//     exponentials -- this shortens each warpgroup's chain softmax -> P V ->
+//     Q K^T, which bounds the kernel.
 //   * Softmax warpgroups w = 0, 1 (warps 4w..4w+3; thread t owns row t of
 //     query tile w, which is TMEM lane t): tcgen05.ld of S_w, mask, row
 //     maximum (3-input max), p = 2^(s*scale*log2(e) - m) with the scale
 //     folded into a packed FFMA2, packed row sums, fp16 pack of p written
-//     back over S_w (in two released halves with SPLIT_P).  O_w is rescaled
-//     lazily, before the tile's P is released: only when a row's maximum grows
+//     back over S_w (in two released halves with SPLIT_P; SPLIT_P = 2 runs
+//     the O rescale between the halves, 1 before the exponentials).  O_w is
+//     rescaled lazily, before the tile's P is released: only when a row's
+//     maximum grows
 //     by more than kTau (log2 units) over the reference it was using;
 //     otherwise p is taken against the stale reference, which is exact
 //     because p, d and o share it (the conditional rescale the page credits
@@ -115,12 +118,13 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // p = 2^(s*sl2 - m_ref) for one 128-column score row (sr, TMEM columns
 // tS .. tS + 127), packed to fp16 pairs (FP8: E4M3 quadruples) and written
 // back over S in two halves of 64 keys; with SPLIT_P each half is released
-// to the MMA thread as soon as it is in TMEM.  Returns the row sum of the fp32 p.  MASK: 0 = columns
+// to the MMA thread as soon as it is in TMEM, `mid` running just before the
+// first release.  Returns the row sum of the fp32 p.  MASK: 0 = columns
 // >= lim masked when `masked` (decided at run time), 1 = none masked, 2 =
 // columns >= lim masked.
-template <int MASK, int EMU, bool SPLIT_P, bool FP8>
+template <int MASK, int EMU, int SPLIT_P, bool FP8, typename Mid>
 __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2v, float2 nm, bool masked, int lim,
-                                         uint32_t tS, uint64_t* p_half, uint64_t* p_full) {
+                                         uint32_t tS, uint64_t* p_half, uint64_t* p_full, Mid&& mid) {
   const bool mk = MASK == 2 || (MASK == 0 && masked);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -164,6 +168,7 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
       tmem_st32(tS + h * 32, pk);
     }
     if constexpr (SPLIT_P) {
+      if (h == 0) mid();  // runs before the first half is released
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(h ? p_full : p_half);
@@ -181,14 +186,14 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
 // recorded since the last attn_get_status().
 __device__ int g_attn_status;
 
-template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV, bool FP8>
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
                 float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_l, int Nq, int Nk,
                 float sl2, float o_scale, uint64_t timeout_ns,
                 int drop_tile) {
-  static_assert(!FP8 || (HD == 128 && !SPLIT_P), "the E4M3 kernel is built for D = 128 only");
+  static_assert(!FP8 || HD == 128, "the E4M3 kernel is built for D = 128 only");
   using L = Layout<HD, NS, FP8>;
   constexpr uint32_t TB = L::kTileBytes;
 
@@ -447,7 +452,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       if (__any_sync(0xffffffffu, resc)) {
         const float2 al = make_float2(alpha, alpha);
-        if constexpr (SPLIT_P) {
+        if constexpr (SPLIT_P == 1) {
           // Rescale runs before the exponentials, with the score row live:
           // 8-column chunks keep it light on registers.
 #pragma unroll 1
@@ -464,8 +469,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tmem_st8(tO + c * 8, orr);
           }
         } else {
-          // Rescale runs after the exponentials (the score row is dead):
-          // full 32-column chunks, unrolled.
+          // Rescale runs after the exponentials (the score row is dead), or
+          // between the two halves of P (half of it live): full 32-column
+          // chunks, unrolled.
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t orr[32];
@@ -521,9 +527,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         m_ref = mt;
         dsum *= alpha;
       }
-      if constexpr (SPLIT_P) {
+      if constexpr (SPLIT_P == 1) {
         if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
       }
+      bool mid_ok = true;
+      auto mid = [&]() {
+        if constexpr (SPLIT_P == 2) {
+          if (j >= 1) mid_ok = rescale_o(j, resc, alpha);
+        }
+      };
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const float2 nm = make_float2(neg_m, neg_m);
 
@@ -532,11 +544,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // was measured to pay (causal, D = 64); the non-causal D = 128 kernel
       // keeps one loop with the mask decided at run time.
       if constexpr (CAUSAL || HD == 64) {
-        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8>(sr, sl2v, nm, true, lim, tS, &p_half[wg], &p_full[wg])
-                       : exp_row<1, EMU, SPLIT_P, FP8>(sr, sl2v, nm, false, lim, tS, &p_half[wg], &p_full[wg]);
+        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8>(sr, sl2v, nm, true, lim, tS, &p_half[wg], &p_full[wg], mid)
+                       : exp_row<1, EMU, SPLIT_P, FP8>(sr, sl2v, nm, false, lim, tS, &p_half[wg], &p_full[wg], mid);
       } else {
-        dsum += exp_row<0, EMU, SPLIT_P, FP8>(sr, sl2v, nm, masked, lim, tS, &p_half[wg], &p_full[wg]);
+        dsum += exp_row<0, EMU, SPLIT_P, FP8>(sr, sl2v, nm, masked, lim, tS, &p_half[wg], &p_full[wg], mid);
       }
+      if (!(ok = mid_ok)) break;
       if constexpr (!SPLIT_P) {
         if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
         tmem_st_wait();
@@ -779,7 +792,7 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-template <int HD, bool CAUSAL, int NS, bool SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false>
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
                float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
                uint64_t timeout_ns, int drop, float o_scale = 1.0f) {
@@ -800,13 +813,13 @@ int dispatch_fwd(int D, int causal, const CUtensorMap& mq, const CUtensorMap& mk
                  void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
                  cudaStream_t st, uint64_t timeout, int drop) {
   if (D == 64)
-    return causal ? launch_fwd<64, true, 4, true, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+    return causal ? launch_fwd<64, true, 4, 2, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
                                                                    splits, st, timeout, drop)
-                  : launch_fwd<64, false, 4, true, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                  : launch_fwd<64, false, 4, 2, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                     sl2, splits, st, timeout, drop);
-  return causal ? launch_fwd<128, true, 2, false, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+  return causal ? launch_fwd<128, true, 2, 2, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                     sl2, splits, st, timeout, drop)
-                : launch_fwd<128, false, 2, false, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                : launch_fwd<128, false, 2, 2, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                      sl2, splits, st, timeout, drop);
 }
 
@@ -1053,9 +1066,9 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                                                                           static_cast<uint8_t*>(workspace), Nk, ldk);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ECUDA;
   const float sl2 = scale * q_descale * k_descale * 1.4426950408889634f;
-  return causal ? launch_fwd<128, true, 4, false, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
+  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
                                                                   sl2, 1, st, timeout, drop, v_descale)
-                : launch_fwd<128, false, 4, false, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
+                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
                                                                    sl2, 1, st, timeout, drop, v_descale);
 }
 
