@@ -17,7 +17,7 @@ ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_ESCRATC
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 # Every symbol the C header declares; the CPU tests check they are exported.
-EXPORTS = ("attn_fwd", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
+EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
            "attn_fwd_splitkv_noalloc", "attn_fwd_fp8", "attn_fp8_workspace_bytes", "attn_debug_pack_e4m3",
            "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
 
@@ -45,6 +45,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd.restype = i32
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, vp]
+            lib.attn_fwd_host.restype = i32
+            lib.attn_fwd_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp]
             lib.attn_fwd_splitkv.restype = i32
             lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, i32, vp, ctypes.c_size_t, vp]
@@ -86,6 +88,14 @@ def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None
     return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
                                    int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
                                    stream)
+
+
+def attn_fwd_host(qh: int, kh: int, vh: int, oh: int, lh: int | None, qd: int, kd: int, vd: int, od: int,
+                  ld: int | None, B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+                  num_chunks: int, stream: int | None) -> int:
+    """Direct call of the host-buffer entry point (raw host and device pointers)."""
+    return load_library().attn_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, int(B), int(H), int(Nq), int(Nk),
+                                        int(D), float(scale), int(bool(causal)), int(num_chunks), stream)
 
 
 def attn_fwd_splitkv(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None,
@@ -164,6 +174,47 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd")
     return out, lse
+
+
+def fwd_host(q, k, v, scale: float | None = None, causal: bool = False, num_chunks: int = 0,
+             device=None, dev_buffers=None, out=None, lse=None, want_lse: bool = True):
+    """attn_fwd on CPU tensors (pinned for overlap); returns host (o, lse).
+
+    q, k, v: contiguous CPU float16 tensors [B,H,N,D].  dev_buffers: an
+    optional (q, k, v, o, lse) tuple of CUDA tensors of the full sizes,
+    allocated here when not given.  The call synchronises the current
+    stream before returning, so the host outputs are ready."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (isinstance(t, torch.Tensor) and not t.is_cuda and t.dtype == torch.float16):
+            raise TypeError(f"{name} must be a CPU float16 tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D [B,H,N,D] tensor")
+    B, H, Nq, D = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError("k and v must be [B,H,Nk,D] with q's B, H and D")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if dev_buffers is None:
+        dev_buffers = (torch.empty_like(q, device=device), torch.empty_like(k, device=device),
+                       torch.empty_like(v, device=device), torch.empty_like(q, device=device),
+                       torch.empty((B, H, Nq), dtype=torch.float32, device=device) if want_lse else None)
+    qd, kd, vd, od, ld = dev_buffers
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32)
+    stream = _current_stream_ptr(device)
+    code = attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if want_lse else None, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
+                         od.data_ptr(), ld.data_ptr() if want_lse else None, B, H, Nq, Nk, D, scale, causal,
+                         num_chunks, stream)
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_host")
+    torch.cuda.current_stream(device).synchronize()
+    return out, (lse if want_lse else None)
 
 
 def fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, num_splits: int | None = None,

@@ -908,6 +908,35 @@ void* noalloc_scratch_address(int dev) {
   return g_noalloc_addr[dev];
 }
 
+// Streams and events of attn_fwd_host, created once per device on first
+// use (never per call) and kept until the process exits.  One mutex guards
+// the enqueue, so calls from several host threads serialise on them.
+constexpr int kMaxHostChunks = 64;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_comp[2] = {nullptr, nullptr}, s_out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in[kMaxHostChunks] = {}, comp[kMaxHostChunks] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+HostPipe* host_pipe(int dev) {  // call with g_pipe_mu held
+  HostPipe& p = g_pipe[dev];
+  if (p.ready) return &p;
+  const unsigned f = cudaEventDisableTiming;
+  bool ok = cudaStreamCreateWithFlags(&p.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.s_comp[0], cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.s_comp[1], cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p.start, f) == cudaSuccess && cudaEventCreateWithFlags(&p.done, f) == cudaSuccess;
+  for (int c = 0; ok && c < kMaxHostChunks; ++c)
+    ok = cudaEventCreateWithFlags(&p.in[c], f) == cudaSuccess && cudaEventCreateWithFlags(&p.comp[c], f) == cudaSuccess;
+  if (!ok) return nullptr;  // what was created stays for the next attempt to reuse or leak; rare
+  p.ready = true;
+  return &p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1016,6 +1045,78 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
   if (r != ATTN_OK) return r;
   return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
                  : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
+}
+
+int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                  void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int H, int Nq, int Nk,
+                  int D, float scale, int causal, int num_chunks, void* stream) {
+  if (!q_host || !k_host || !v_host || !o_host) return ATTN_EINVAL;
+  if ((lse_host == nullptr) != (lse_dev == nullptr)) return ATTN_EINVAL;
+  if (num_chunks < 0 || num_chunks > kMaxHostChunks) return ATTN_EINVAL;
+  bool empty = false;
+  const int rc = check_args(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Nq, Nk, D, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  const int BH = B * H;
+  const size_t qb = static_cast<size_t>(BH) * Nq * D * 2, kb = static_cast<size_t>(BH) * Nk * D * 2;
+  if (ranges_overlap(q_dev, qb, k_dev, kb) || ranges_overlap(q_dev, qb, v_dev, kb) ||
+      ranges_overlap(k_dev, kb, v_dev, kb))
+    return ATTN_EUNSUPPORTED;  // the device copies of the inputs are written here
+  const int sms = device_sms();
+  if (sms <= 0) return -sms;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  const int chunks = std::max(1, std::min(num_chunks == 0 ? 32 : num_chunks, BH));
+  uint64_t timeout;
+  int drop;
+  debug_settings(&timeout, &drop);
+  const float sl2 = scale * 1.4426950408889634f;
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* p = host_pipe(dev);
+  if (!p) return ATTN_ECUDA;
+  // Every internal stream starts after the work already queued on `user`
+  // (which may still use the device buffers), and `user` resumes when the
+  // last output has reached host memory.
+  if (cudaEventRecord(p->start, user) != cudaSuccess || cudaStreamWaitEvent(p->s_in, p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->s_comp[0], p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->s_comp[1], p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->s_out, p->start, 0) != cudaSuccess)
+    return ATTN_ECUDA;
+  const auto H2D = cudaMemcpyHostToDevice;
+  const auto D2H = cudaMemcpyDeviceToHost;
+  for (int c = 0; c < chunks; ++c) {
+    // Chunks alternate between two compute streams, so that the next
+    // chunk's CTAs take the SMs the current one frees in its last wave.
+    cudaStream_t sc = p->s_comp[c & 1];
+    // heads [h0, h1) of the flattened B*H: contiguous in every tensor
+    const int h0 = static_cast<int>(static_cast<int64_t>(BH) * c / chunks);
+    const int h1 = static_cast<int>(static_cast<int64_t>(BH) * (c + 1) / chunks);
+    const int nb = h1 - h0;
+    const size_t qo = static_cast<size_t>(h0) * Nq * D * 2, ko = static_cast<size_t>(h0) * Nk * D * 2;
+    const size_t qn = static_cast<size_t>(nb) * Nq * D * 2, kn = static_cast<size_t>(nb) * Nk * D * 2;
+    const size_t lo = static_cast<size_t>(h0) * Nq, ln = static_cast<size_t>(nb) * Nq * 4;
+    auto at = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
+    auto atw = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
+    if (cudaMemcpyAsync(atw(q_dev, qo), at(q_host, qo), qn, H2D, p->s_in) != cudaSuccess ||
+        cudaMemcpyAsync(atw(k_dev, ko), at(k_host, ko), kn, H2D, p->s_in) != cudaSuccess ||
+        cudaMemcpyAsync(atw(v_dev, ko), at(v_host, ko), kn, H2D, p->s_in) != cudaSuccess ||
+        cudaEventRecord(p->in[c], p->s_in) != cudaSuccess || cudaStreamWaitEvent(sc, p->in[c], 0) != cudaSuccess)
+      return ATTN_ECUDA;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, at(q_dev, qo), nb, Nq, D) || !make_map(&mk, at(k_dev, ko), nb, Nk, D) ||
+        !make_map(&mv, at(v_dev, ko), nb, Nk, D))
+      return ATTN_ECUDA;
+    const int r = dispatch_fwd<false>(D, causal, mq, mk, mv, atw(o_dev, qo), lse_dev ? lse_dev + lo : nullptr,
+                                      nullptr, nullptr, nb, Nq, Nk, sl2, 1, sc, timeout, drop);
+    if (r != ATTN_OK) return r;
+    if (cudaEventRecord(p->comp[c], sc) != cudaSuccess || cudaStreamWaitEvent(p->s_out, p->comp[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(atw(o_host, qo), at(o_dev, qo), qn, D2H, p->s_out) != cudaSuccess ||
+        (lse_host && cudaMemcpyAsync(lse_host + lo, lse_dev + lo, ln, D2H, p->s_out) != cudaSuccess))
+      return ATTN_ECUDA;
+  }
+  if (cudaEventRecord(p->done, p->s_out) != cudaSuccess || cudaStreamWaitEvent(user, p->done, 0) != cudaSuccess)
+    return ATTN_ECUDA;
+  return ATTN_OK;
 }
 
 size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D) {

@@ -82,6 +82,43 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Nk, int D, float scale, int causal, void* stream);
 
 /*
+ * attn_fwd_host -- attn_fwd for tensors in HOST memory: copies Q, K and V
+ * to the caller's device buffers, runs the forward and copies O and LSE back,
+ * with the three overlapped.  The heads (the flattened B*H) are cut into
+ * num_chunks contiguous groups; chunk c's host-to-device copy, its forward
+ * and its device-to-host copy run on internal streams (one for the copies
+ * in, two for the forwards, taken in turn so that consecutive chunks share
+ * the SMs at their boundary, one for the copies out), so chunk c+1 is copied
+ * in while chunk c is computed and chunk c-1 copied out.  (The
+ * pages have no counterpart: this is the library's end-to-end entry point.)
+ *
+ *   q_host, k_host, v_host, o_host, lse_host  host tensors, same layouts as
+ *          attn_fwd.  Page-locked (pinned) memory is needed for the copies
+ *          to overlap; pageable memory works, slower.  lse_host may be NULL
+ *          (then lse_dev must be NULL too).
+ *   q_dev, k_dev, v_dev, o_dev, lse_dev  device buffers of the full sizes,
+ *          with attn_fwd's alignment and overlap rules (q/k/v also must not
+ *          overlap one another); the inputs are copied into them and the
+ *          outputs computed there, so they hold the same data as after
+ *          attn_fwd when the call completes.
+ *   num_chunks  1 .. 64, or 0 for the default (32); capped at B*H.
+ *   B, H, Nq, Nk, D, scale, causal: as attn_fwd.
+ *   stream  the work starts after everything already queued on `stream`
+ *          and `stream` waits for the last output copy: synchronise it
+ *          before reading o_host / lse_host.
+ *
+ * The internal streams and events are created once per device, on the
+ * first call (make that call before any stream capture), and reused; calls
+ * from several host threads serialise on them.  Nothing is allocated per
+ * call.  Errors: as attn_fwd, plus ATTN_EINVAL for a null host tensor,
+ * lse_host and lse_dev not both given or both NULL, or num_chunks outside
+ * 0..64.
+ */
+int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                  void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int H, int Nq,
+                  int Nk, int D, float scale, int causal, int num_chunks, void* stream);
+
+/*
  * attn_fwd_splitkv -- the same forward, with the keys of every query tile
  * divided into num_splits contiguous shares that separate CTAs compute in
  * parallel, followed by a merge.  This is the split-KV / Flash-Decoding

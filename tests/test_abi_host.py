@@ -159,3 +159,17 @@ def test_debug_pack_validation(lib):
     assert lib.attn_debug_pack_e4m3(None, None, 4, None) == attn.ATTN_EINVAL
     assert lib.attn_debug_pack_e4m3(A, A, -1, None) == attn.ATTN_EINVAL
     assert lib.attn_debug_pack_e4m3(A, A, 0, None) == attn.ATTN_OK
+
+
+@pytest.mark.parametrize("args,code", [
+    # qh, kh, vh, oh, lh, qd, kd, vd, od, ld, B, H, Nq, Nk, D, scale, causal, chunks
+    ((0, W, W, W, None, A, A + (1 << 16), A + (2 << 16), 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, 0), attn.ATTN_EINVAL),
+    ((W, W, W, W, W, A, A + (1 << 16), A + (2 << 16), 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, 0), attn.ATTN_EINVAL),
+    ((W, W, W, W, None, A, A + (1 << 16), A + (2 << 16), 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, 65), attn.ATTN_EINVAL),
+    ((W, W, W, W, None, A, A + (1 << 16), A + (2 << 16), 2 * A, None, 1, 1, 8, 8, 96, 0.1, 0, 0), attn.ATTN_EUNSUPPORTED),
+    ((W, W, W, W, None, A, A, A + (2 << 16), 2 * A, None, 1, 1, 8, 8, 64, 0.1, 0, 0), attn.ATTN_EUNSUPPORTED),  # q_dev = k_dev
+    ((W, W, W, W, None, A, A + (1 << 16), A + (2 << 16), A, None, 1, 1, 8, 8, 64, 0.1, 0, 0), attn.ATTN_EUNSUPPORTED),
+    ((W, W, W, W, None, A, A + (1 << 16), A + (2 << 16), 2 * A, None, 0, 1, 8, 8, 64, 0.1, 0, 0), attn.ATTN_OK),
+])
+def test_host_entry_validation_without_device(lib, args, code):
+    assert attn.attn_fwd_host(*args, None) == code
