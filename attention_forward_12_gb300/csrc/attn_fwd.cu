@@ -693,10 +693,13 @@ attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restric
 // V^T for the E4M3 kernel, whose O += P V takes V K-major (keys contiguous):
 // vt[bh][d][key] = v[bh][key][d] for D = 128, rows of ldk bytes (the key
 // count rounded up to 16; the keys in between are written as zero).  One CTA
-// per 128 keys of one head, staged through shared memory.
+// per 128 keys of one head: the tile goes through shared memory as 32-bit
+// words (rows padded to 33 words, so that both phases are free of bank
+// conflicts), and each thread turns four 4 x 4 byte blocks around with byte
+// permutes into 16 consecutive keys of 4 rows of V^T.
 __global__ void __launch_bounds__(256)
 attn_fp8_transpose_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt, int Nk, int ldk) {
-  __shared__ __align__(16) uint8_t tile[128][128 + 16];
+  __shared__ uint32_t tile[128][33];
   const size_t bh = blockIdx.y;
   const int k0 = blockIdx.x * 128;
   const uint8_t* src = v + bh * static_cast<size_t>(Nk) * 128;
@@ -704,23 +707,32 @@ attn_fp8_transpose_v_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__
     const int key = c >> 3, part = c & 7;
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
     if (k0 + key < Nk) val = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(k0 + key) * 128 + part * 16);
-    *reinterpret_cast<uint4*>(&tile[key][part * 16]) = val;
+    tile[key][4 * part] = val.x;
+    tile[key][4 * part + 1] = val.y;
+    tile[key][4 * part + 2] = val.z;
+    tile[key][4 * part + 3] = val.w;
   }
   __syncthreads();
-  uint8_t* dst = vt + bh * 128 * static_cast<size_t>(ldk);
-  for (int c = threadIdx.x; c < 1024; c += blockDim.x) {
-    const int d = c >> 3, kp = c & 7;
-    const int key = k0 + kp * 16;
-    if (key >= ldk) continue;
-    uint32_t w[4];
+  const int db = threadIdx.x & 31;  // rows 4 db .. 4 db + 3 of V^T
+  const int kb = threadIdx.x >> 5;  // keys k0 + 16 kb .. + 15
+  if (k0 + 16 * kb >= ldk) return;
+  uint32_t out[4][4];  // [row j][group g]: keys 4g .. 4g + 3 of row 4 db + j
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = kp * 16 + 4 * q;
-      w[q] = static_cast<uint32_t>(tile[r][d]) | (static_cast<uint32_t>(tile[r + 1][d]) << 8) |
-             (static_cast<uint32_t>(tile[r + 2][d]) << 16) | (static_cast<uint32_t>(tile[r + 3][d]) << 24);
-    }
-    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(d) * ldk + key) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int g = 0; g < 4; ++g) {
+    const int r = 16 * kb + 4 * g;
+    const uint32_t w0 = tile[r][db], w1 = tile[r + 1][db], w2 = tile[r + 2][db], w3 = tile[r + 3][db];
+    const uint32_t a = __byte_perm(w0, w1, 0x5140), b = __byte_perm(w2, w3, 0x5140);  // bytes 0, 1
+    const uint32_t c = __byte_perm(w0, w1, 0x7362), d = __byte_perm(w2, w3, 0x7362);  // bytes 2, 3
+    out[0][g] = __byte_perm(a, b, 0x5410);
+    out[1][g] = __byte_perm(a, b, 0x7632);
+    out[2][g] = __byte_perm(c, d, 0x5410);
+    out[3][g] = __byte_perm(c, d, 0x7632);
   }
+  uint8_t* dst = vt + bh * 128 * static_cast<size_t>(ldk) + k0 + 16 * kb;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(4 * db + j) * ldk) =
+        make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
 }
 
 // The softmax's E4M3 packing on its own, for tests: out[i] packs in[4i..4i+3].

@@ -35,3 +35,45 @@ def test_dropped_load_times_out_and_context_survives():
     assert attn.get_status() == attn.ATTN_OK
     O, L = oracle.attn_full(qn, kn, vn, 1.0 / math.sqrt(D), False)
     compare(o.cpu().numpy(), lse.cpu().numpy(), O, L, "after timeout")
+
+
+def test_dropped_load_times_out_in_the_e4m3_forward():
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    attn.build()
+    q8, k8, v8 = synth.make_qkv_e4m3(1, 2, 512, 512, 128, seed=22)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (q8, k8, v8))
+    assert attn.get_status() == attn.ATTN_OK
+    try:
+        assert attn.debug_set(50_000_000, 1) == attn.ATTN_OK
+        attn.fwd_fp8(q, k, v)
+        torch.cuda.synchronize()
+        assert attn.get_status() == attn.ATTN_ETIMEOUT
+    finally:
+        attn.debug_set(2_000_000_000, -1)
+    o, lse = attn.fwd_fp8(q, k, v)
+    torch.cuda.synchronize()
+    assert attn.get_status() == attn.ATTN_OK
+    O, L = oracle.attn_full_e4m3(q8, k8, v8, 128 ** -0.5, False)
+    og = o.cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(og - O) / np.linalg.norm(O) <= 0.05
+    assert np.abs(lse.cpu().numpy() - L).max() <= 1e-3
+
+
+def test_dropped_load_times_out_in_the_host_entry():
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    attn.build()
+    qn, kn, vn = synth.make_qkv(1, 4, 256, 256, 64, seed=23)
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (qn, kn, vn))
+    assert attn.get_status() == attn.ATTN_OK
+    try:
+        assert attn.debug_set(50_000_000, 1) == attn.ATTN_OK
+        attn.fwd_host(qh, kh, vh, num_chunks=2)
+        assert attn.get_status() == attn.ATTN_ETIMEOUT
+    finally:
+        attn.debug_set(2_000_000_000, -1)
+    oh, lh = attn.fwd_host(qh, kh, vh, num_chunks=2)
+    assert attn.get_status() == attn.ATTN_OK
+    O, L = oracle.attn_full(qn, kn, vn, 1.0 / math.sqrt(64), False)
+    compare(oh.numpy(), lh.numpy(), O, L, "host entry after timeout")
