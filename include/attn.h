@@ -24,7 +24,8 @@
  *     they multiply V (as the page's C->A repack rounds P with cvt.rn).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous on that stream; they perform no host synchronisation
- *     and no allocation.
+ *     and no allocation, so they can be captured in a CUDA graph (make one
+ *     ordinary call on the device first: it sets the kernels' attributes).
  *   - Return values are ATTN_* codes below.  Argument errors are detected on
  *     the host before anything is enqueued.
  */
