@@ -49,8 +49,10 @@
 //     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
 //
-// TMEM (512 columns): S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+D),
-// O_1 [384,384+D).
+// TMEM (512 columns): at D = 128, S_0/P_0 [0,128), S_1/P_1 [128,256),
+// O_0 [256,384), O_1 [384,512).  At D = 64 three score slots [0,128),
+// [128,256), [256,384) rotate between the two query tiles (so a tile's next
+// scores do not wait for its own P V), O_0 [384,448), O_1 [448,512).
 //
 // Every mbarrier wait is bounded (see WaitCtl): a wait that runs out raises
 // the CTA's abort flag and the device status word; the CTA then drains its
@@ -92,7 +94,9 @@ struct Layout {
   static constexpr int kChunks = HD * kElem / 128;            // 128-byte column blocks per row
   static constexpr int kChunkElems = 128 / kElem;
   static constexpr uint32_t kTileBytes = kBlockM * HD * kElem;  // one Q, K or V tile
-  static constexpr int kBars = 1 + 4 * NS + 2 + 2 + 2 + 2 + 1;
+  // q_full, k/v full/empty[NS], s_full/p_half/p_full[3] (one per TMEM score
+  // slot), o_done[4], drain
+  static constexpr int kBars = 1 + 4 * NS + 3 * 3 + 4 + 1;
   static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
 };
 
@@ -186,7 +190,7 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
 // recorded since the last attn_get_status().
 __device__ int g_attn_status;
 
-template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8>
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8, int SLOTS>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
@@ -208,11 +212,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   uint64_t* k_empty = k_full + NS;
   uint64_t* v_full = k_empty + NS;
   uint64_t* v_empty = v_full + NS;
-  uint64_t* s_full = v_empty + NS;  // [2] S_w landed in TMEM
-  uint64_t* p_half = s_full + 2;    // [2] first 64 columns of P_w written (and O_w rescaled)
-  uint64_t* p_full = p_half + 2;    // [2] all of P_w written over S_w
-  uint64_t* o_done = p_full + 2;    // [2] one phase per completed O_w += P_w V
-  uint64_t* drain = o_done + 2;     // abort path only
+  uint64_t* s_full = v_empty + NS;  // [SLOTS] S landed in TMEM score slot b
+  uint64_t* p_half = s_full + 3;    // [SLOTS] first 64 keys of P written over slot b (and O rescaled)
+  uint64_t* p_full = p_half + 3;    // [SLOTS] all of P written over slot b
+  uint64_t* o_done = p_full + 3;    // [4] completed O_w += P_w V_j: SLOTS = 2: [w], one phase per
+                                    // product; SLOTS = 3: [2w + (j & 1)], one phase per two
+  uint64_t* drain = o_done + 4;     // abort path only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* last_k = abort_flag + 1;     // [NS] last tile loaded per stage (abort drain)
@@ -269,12 +274,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       last_k[s] = -1;
       last_v[s] = -1;
     }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(&s_full[w], 1);
-      mbar_init(&p_half[w], kBlockM);
-      mbar_init(&p_full[w], kBlockM);
-      mbar_init(&o_done[w], 1);
+    for (int b = 0; b < SLOTS; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_half[b], kBlockM);
+      mbar_init(&p_full[b], kBlockM);
     }
+    for (int b = 0; b < 4; ++b) mbar_init(&o_done[b], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -288,6 +293,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
 
   const uint32_t tmem = *tmem_slot;
+  // TMEM score slots: one per query tile (SLOTS = 2: S_w at column 128 w),
+  // or three that the two query tiles' score tiles rotate through (SLOTS =
+  // 3, D = 64: slots at 0, 128, 256).  O_w after the slots.
+  constexpr uint32_t kOCol = SLOTS == 3 ? 384 : 256;
+  constexpr uint32_t kOStride = SLOTS == 3 ? HD : 128;
+  static_assert(SLOTS == 2 || (SLOTS == 3 && kOCol + 2 * HD <= kTmemCols), "TMEM budget");
+  // With three slots the score tiles are numbered in the order the tensor
+  // core computes them -- (tile 0, Q tile 0), (0, 1), (1, 0), (1, 1), ...,
+  // then the longer query tile's remaining ones -- and item n uses slot
+  // n % 3.  Item n + 3 reuses the slot once O += P V of item n is issued:
+  // a query tile's next scores wait for the other tile's product, not for
+  // its own.
+  const int mmin = min(nkv0, nkv1);
+  const int wlong = nkv0 > nkv1 ? 0 : 1;
+  const int nitems = nkv0 + nkv1;
   const WaitCtl wc{abort_flag, &g_attn_status, timeout_ns};
 
   if (warp == kProducerWarp) {
@@ -358,8 +378,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     constexpr int kPvSteps = kBlockN * L::kElem / 32;  // 32 bytes of keys per product
     // S_w = Q_w K^T of stage s: both operands K-major, 128B swizzle; the
     // reduction over D runs in steps of 16 (32 bytes inside a swizzle row).
-    auto issue_s = [&](int w, int s) {
-      const uint32_t dS = tmem + w * 128;
+    auto issue_s = [&](int w, int s, int slot) {
+      const uint32_t dS = tmem + slot * 128;
       const uint64_t a = dQ + ((w * TB) >> 4);
       const uint64_t b = dK + ((s * TB) >> 4);
 #pragma unroll
@@ -370,22 +390,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         else
           umma_ss_warp(dS, a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
       }
-      umma_commit_warp(&s_full[w]);
+      umma_commit_warp(&s_full[slot]);
     };
     // O_w += P_w V of stage s: P (fp16, two per column) from TMEM as the A
     // operand; V MN-major in shared memory (rows = keys, 128 bytes of D per
     // row; LBO = next 64 columns of D, SBO = next 8 keys).  The first 64 keys
     // go as soon as the softmax has released the first half of P, so the
     // tensor core works while the second half is being computed.
-    auto issue_pv = [&](int w, int j, int s) -> bool {
-      const uint32_t aP = tmem + w * 128;
-      const uint32_t dO = tmem + 256 + w * 128;
+    auto issue_pv = [&](int w, int j, int s, int slot, uint32_t par) -> bool {
+      const uint32_t aP = tmem + slot * 128;
+      const uint32_t dO = tmem + kOCol + w * kOStride;
       const uint64_t b = dV + ((s * TB) >> 4);
       constexpr int kParts = SPLIT_P ? 2 : 1;
 #pragma unroll
       for (int part = 0; part < kParts; ++part) {
         const bool last = part == kParts - 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(last ? &p_full[w] : &p_half[w], j & 1, wc, ATTN_ETIMEOUT))) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(last ? &p_full[slot] : &p_half[slot], par, wc, ATTN_ETIMEOUT)))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = part * kPvSteps / kParts; kk < (part + 1) * kPvSteps / kParts; ++kk) {
@@ -397,7 +418,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             umma_ts_warp(dO, aP + kk * 8, b + ((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
       }
-      umma_commit_warp(&o_done[w]);
+      umma_commit_warp(&o_done[SLOTS == 3 ? 2 * w + (j & 1) : w]);
       return true;
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -405,27 +426,68 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       return true;
     };
-    bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
-    if (ok) {
-      if (nkv0 > 0) issue_s(0, 0);
-      if (nkv1 > 0) issue_s(1, 0);
-      umma_commit_warp(&k_empty[0]);
-    }
-    for (int j = 0; j < nkv && ok; ++j) {
-      const int s = j % NS;
-      const int s1 = (j + 1) % NS;
-      const bool more = j + 1 < nkv;
-      if (!(ok = wait_all(&v_full[s], (j / NS) & 1))) break;
-      if (j < nkv0 && !(ok = issue_pv(0, j, s))) break;
-      if (more) {
-        if (!(ok = wait_all(&k_full[s1], ((j + 1) / NS) & 1))) break;
-        if (j + 1 < nkv0) issue_s(0, s1);
+    if constexpr (SLOTS == 2) {
+      bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+      if (ok) {
+        if (nkv0 > 0) issue_s(0, 0, 0);
+        if (nkv1 > 0) issue_s(1, 0, 1);
+        umma_commit_warp(&k_empty[0]);
       }
-      if (j < nkv1 && !(ok = issue_pv(1, j, s))) break;
-      umma_commit_warp(&v_empty[s]);
-      if (more) {
-        if (j + 1 < nkv1) issue_s(1, s1);
-        umma_commit_warp(&k_empty[s1]);
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int s = j % NS;
+        const int s1 = (j + 1) % NS;
+        const bool more = j + 1 < nkv;
+        if (!(ok = wait_all(&v_full[s], (j / NS) & 1))) break;
+        if (j < nkv0 && !(ok = issue_pv(0, j, s, 0, j & 1))) break;
+        if (more) {
+          if (!(ok = wait_all(&k_full[s1], ((j + 1) / NS) & 1))) break;
+          if (j + 1 < nkv0) issue_s(0, s1, 0);
+        }
+        if (j < nkv1 && !(ok = issue_pv(1, j, s, 1, j & 1))) break;
+        umma_commit_warp(&v_empty[s]);
+        if (more) {
+          if (j + 1 < nkv1) issue_s(1, s1, 1);
+          umma_commit_warp(&k_empty[s1]);
+        }
+      }
+    } else {
+      // Items in order: S of item n + 3 follows O += P V of item n.  A key
+      // tile's K stage is released after its last score item, its V stage
+      // after its last product.
+      auto tile_of = [&](int n, int& j, int& w) {
+        if (n < 2 * mmin) {
+          j = n >> 1;
+          w = n & 1;
+        } else {
+          j = mmin + (n - 2 * mmin);
+          w = wlong;
+        }
+      };
+      auto last_item = [&](int j) { return j < mmin ? 2 * j + 1 : 2 * mmin + (j - mmin); };
+      int k_seen = -1, v_seen = -1;  // last key tile whose K / V landing was waited for
+      auto s_item = [&](int n) -> bool {
+        int j, w;
+        tile_of(n, j, w);
+        if (j > k_seen) {
+          if (!wait_all(&k_full[j % NS], (j / NS) & 1)) return false;
+          k_seen = j;
+        }
+        issue_s(w, j % NS, n % 3);
+        if (n == last_item(j)) umma_commit_warp(&k_empty[j % NS]);
+        return true;
+      };
+      bool ok = wait_all(q_full, 0);
+      for (int n = 0; n < 3 && n < nitems && ok; ++n) ok = s_item(n);
+      for (int n = 0; n < nitems && ok; ++n) {
+        int j, w;
+        tile_of(n, j, w);
+        if (j > v_seen) {
+          if (!(ok = wait_all(&v_full[j % NS], (j / NS) & 1))) break;
+          v_seen = j;
+        }
+        if (!(ok = issue_pv(w, j, j % NS, n % 3, (n / 3) & 1))) break;
+        if (n == last_item(j)) umma_commit_warp(&v_empty[j % NS]);
+        if (n + 3 < nitems && !(ok = s_item(n + 3))) break;
       }
     }
     __syncwarp();
@@ -437,8 +499,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int i = rw + row;
     const int my_nkv = wg ? nkv1 : nkv0;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + wg * 128 + lane_off;
-    const uint32_t tO = tmem + 256 + wg * 128 + lane_off;
+    const uint32_t tO = tmem + kOCol + wg * kOStride + lane_off;
     const int row_lim = CAUSAL ? min(Nk, i + 1) : Nk;  // admissible keys: [0, row_lim)
     const float2 sl2v = make_float2(sl2, sl2);
     float m_ref = -INFINITY;  // reference maximum, log2 units of the scaled score
@@ -448,7 +509,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // (in steady state it completed long ago).  The rescale itself is rare
     // (lazy), except on sharply peaked rows whose maximum keeps growing.
     auto rescale_o = [&](int j, bool resc, float alpha) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT))) return false;
+      if constexpr (SLOTS == 3) {
+        // With rotating slots this tile's scores may be ready before the
+        // previous tile's product is even issued, so the softmax waits for
+        // that product only when it must rescale.  Parity waits on the
+        // alternating barriers are exact: the product two before (j - 3)
+        // has completed -- the commit of this tile's S follows the issue
+        // of every product up to three items back -- and the one after
+        // (j + 1) cannot start before this tile's P is released.
+        if (!__any_sync(0xffffffffu, resc)) return true;
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[2 * wg + ((j - 1) & 1)], ((j - 1) >> 1) & 1, wc,
+                                               ATTN_ETIMEOUT)))
+          return false;
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT))) return false;
+      }
       tc_fence_after();
       if (__any_sync(0xffffffffu, resc)) {
         const float2 al = make_float2(alpha, alpha);
@@ -491,7 +566,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     };
     bool ok = true;
     for (int j = 0; j < my_nkv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], j & 1, wc, ATTN_ETIMEOUT));
+      // This tile's score slot and the parity of its use (see the item
+      // numbering above; with two slots, slot = query tile).
+      const int n = SLOTS == 3 ? (j < mmin ? 2 * j + wg : 2 * mmin + (j - mmin)) : j;
+      const int slot = SLOTS == 3 ? n % 3 : wg;
+      const uint32_t par = SLOTS == 3 ? (n / 3) & 1 : j & 1;
+      const uint32_t tS = tmem + slot * 128 + lane_off;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], par, wc, ATTN_ETIMEOUT));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -544,20 +625,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // was measured to pay (causal, D = 64); the non-causal D = 128 kernel
       // keeps one loop with the mask decided at run time.
       if constexpr (CAUSAL || HD == 64) {
-        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8>(sr, sl2v, nm, true, lim, tS, &p_half[wg], &p_full[wg], mid)
-                       : exp_row<1, EMU, SPLIT_P, FP8>(sr, sl2v, nm, false, lim, tS, &p_half[wg], &p_full[wg], mid);
+        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8>(sr, sl2v, nm, true, lim, tS, &p_half[slot], &p_full[slot], mid)
+                       : exp_row<1, EMU, SPLIT_P, FP8>(sr, sl2v, nm, false, lim, tS, &p_half[slot], &p_full[slot], mid);
       } else {
-        dsum += exp_row<0, EMU, SPLIT_P, FP8>(sr, sl2v, nm, masked, lim, tS, &p_half[wg], &p_full[wg], mid);
+        dsum += exp_row<0, EMU, SPLIT_P, FP8>(sr, sl2v, nm, masked, lim, tS, &p_half[slot], &p_full[slot], mid);
       }
       if (!(ok = mid_ok)) break;
       if constexpr (!SPLIT_P) {
         if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[wg]);
+        mbar_arrive(&p_full[slot]);
       }
     }
-    if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (my_nkv - 1) & 1, wc, ATTN_ETIMEOUT));
+    if constexpr (SLOTS == 3) {
+      // the last two products, in order (each completion implies the ones before)
+      for (int k = max(0, my_nkv - 2); k < my_nkv && ok; ++k)
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[2 * wg + (k & 1)], (k >> 1) & 1, wc, ATTN_ETIMEOUT));
+    } else {
+      if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (my_nkv - 1) & 1, wc, ATTN_ETIMEOUT));
+    }
     if (ok && my_nkv > 0 && !SPLITKV) {
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
@@ -804,12 +891,12 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false>
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
                float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
                uint64_t timeout_ns, int drop, float o_scale = 1.0f) {
   using L = Layout<HD, NS, FP8>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8>;
+  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
       cudaSuccess)
@@ -825,9 +912,9 @@ int dispatch_fwd(int D, int causal, const CUtensorMap& mq, const CUtensorMap& mk
                  void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
                  cudaStream_t st, uint64_t timeout, int drop) {
   if (D == 64)
-    return causal ? launch_fwd<64, true, 4, 2, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+    return causal ? launch_fwd<64, true, 4, 2, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
                                                                    splits, st, timeout, drop)
-                  : launch_fwd<64, false, 4, 2, kEmu64, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                  : launch_fwd<64, false, 4, 2, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                     sl2, splits, st, timeout, drop);
   return causal ? launch_fwd<128, true, 2, 2, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                     sl2, splits, st, timeout, drop)
