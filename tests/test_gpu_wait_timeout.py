@@ -14,11 +14,12 @@ from gpu_common import compare, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-def test_dropped_load_times_out_and_context_survives():
+@pytest.mark.parametrize("D", [64, 128])
+def test_dropped_load_times_out_and_context_survives(D):
     torch = torch_cuda()
     import attention_forward_12_gb300 as attn
     attn.build()
-    B, H, N, D = 1, 2, 512, 128
+    B, H, N = 1, 2, 512
     qn, kn, vn = synth.make_qkv(B, H, N, N, D, seed=21)
     q, k, v = (torch.from_numpy(x).cuda() for x in (qn, kn, vn))
     assert attn.get_status() == attn.ATTN_OK
