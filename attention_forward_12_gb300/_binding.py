@@ -18,7 +18,7 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 # Every symbol the C header declares; the CPU tests check they are exported.
 EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
-           "attn_fwd_splitkv_noalloc", "attn_fwd_fp8", "attn_fp8_workspace_bytes", "attn_debug_pack_e4m3",
+           "attn_fwd_splitkv_noalloc", "attn_fwd_fp8", "attn_fwd_fp8_host", "attn_fp8_workspace_bytes", "attn_debug_pack_e4m3",
            "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
 
 _lock = threading.Lock()
@@ -57,6 +57,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd_fp8.restype = i32
             lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, f32, f32, f32,
                                          vp, ctypes.c_size_t, vp]
+            lib.attn_fwd_fp8_host.restype = i32
+            lib.attn_fwd_fp8_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, f32, i32, f32, f32, f32, vp,
+                                                          ctypes.c_size_t, i32, vp]
             lib.attn_fp8_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32]
             lib.attn_debug_pack_e4m3.restype = i32
@@ -125,6 +128,17 @@ def attn_fwd_fp8(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | 
     return load_library().attn_fwd_fp8(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq), int(Nk),
                                        int(D), float(scale), int(bool(causal)), float(q_descale),
                                        float(k_descale), float(v_descale), ws_ptr, int(ws_bytes), stream)
+
+
+def attn_fwd_fp8_host(qh: int, kh: int, vh: int, oh: int, lh: int | None, qd: int, kd: int, vd: int, od: int,
+                      ld: int | None, B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+                      q_descale: float, k_descale: float, v_descale: float, ws_ptr: int | None, ws_bytes: int,
+                      num_chunks: int, stream: int | None) -> int:
+    """Direct call of the E4M3 host-buffer entry point (raw pointers)."""
+    return load_library().attn_fwd_fp8_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, int(B), int(H), int(Nq), int(Nk),
+                                            int(D), float(scale), int(bool(causal)), float(q_descale),
+                                            float(k_descale), float(v_descale), ws_ptr, int(ws_bytes),
+                                            int(num_chunks), stream)
 
 
 def fp8_workspace_bytes(B: int, H: int, Nk: int, D: int) -> int:

@@ -1036,6 +1036,118 @@ HostPipe* host_pipe(int dev) {  // call with g_pipe_mu held
   return &p;
 }
 
+// The chunked pipeline of the host-buffer entry points over the flattened
+// B*H heads: chunk c's inputs are copied in on s_in, compute(c, h0, nb,
+// stream) enqueues its forward on one of the two compute streams (taken in
+// turn, so that the next chunk's CTAs take the SMs the current one frees in
+// its last wave), and its outputs are copied out on s_out.  in_elem: bytes
+// per Q/K/V element (O is fp16, LSE fp32).
+template <typename Compute>
+int host_pipeline(int dev, const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                  float* lse_host, void* q_dev, void* k_dev, void* v_dev, const void* o_dev, const float* lse_dev,
+                  int BH, int Nq, int Nk, int D, int in_elem, int chunks, cudaStream_t user, Compute&& compute) {
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* p = host_pipe(dev);
+  if (!p) return ATTN_ECUDA;
+  // Every internal stream starts after the work already queued on `user`
+  // (which may still use the device buffers), and `user` resumes when the
+  // last output has reached host memory.
+  if (cudaEventRecord(p->start, user) != cudaSuccess || cudaStreamWaitEvent(p->s_in, p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->s_comp[0], p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->s_comp[1], p->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->s_out, p->start, 0) != cudaSuccess)
+    return ATTN_ECUDA;
+  const auto H2D = cudaMemcpyHostToDevice;
+  const auto D2H = cudaMemcpyDeviceToHost;
+  auto at = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
+  auto atw = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
+  for (int c = 0; c < chunks; ++c) {
+    cudaStream_t sc = p->s_comp[c & 1];
+    // heads [h0, h0 + nb): contiguous in every tensor
+    const int h0 = static_cast<int>(static_cast<int64_t>(BH) * c / chunks);
+    const int nb = static_cast<int>(static_cast<int64_t>(BH) * (c + 1) / chunks) - h0;
+    const size_t qi = static_cast<size_t>(in_elem) * Nq * D, ki = static_cast<size_t>(in_elem) * Nk * D;
+    const size_t oo = static_cast<size_t>(h0) * Nq * D * 2, on = static_cast<size_t>(nb) * Nq * D * 2;
+    const size_t lo = static_cast<size_t>(h0) * Nq, ln = static_cast<size_t>(nb) * Nq * 4;
+    if (cudaMemcpyAsync(atw(q_dev, h0 * qi), at(q_host, h0 * qi), nb * qi, H2D, p->s_in) != cudaSuccess ||
+        cudaMemcpyAsync(atw(k_dev, h0 * ki), at(k_host, h0 * ki), nb * ki, H2D, p->s_in) != cudaSuccess ||
+        cudaMemcpyAsync(atw(v_dev, h0 * ki), at(v_host, h0 * ki), nb * ki, H2D, p->s_in) != cudaSuccess ||
+        cudaEventRecord(p->in[c], p->s_in) != cudaSuccess || cudaStreamWaitEvent(sc, p->in[c], 0) != cudaSuccess)
+      return ATTN_ECUDA;
+    const int r = compute(c, h0, nb, sc);
+    if (r != ATTN_OK) return r;
+    if (cudaEventRecord(p->comp[c], sc) != cudaSuccess || cudaStreamWaitEvent(p->s_out, p->comp[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(atw(o_host, oo), at(o_dev, oo), on, D2H, p->s_out) != cudaSuccess ||
+        (lse_host && cudaMemcpyAsync(lse_host + lo, lse_dev + lo, ln, D2H, p->s_out) != cudaSuccess))
+      return ATTN_ECUDA;
+  }
+  if (cudaEventRecord(p->done, p->s_out) != cudaSuccess || cudaStreamWaitEvent(user, p->done, 0) != cudaSuccess)
+    return ATTN_ECUDA;
+  return ATTN_OK;
+}
+
+// Argument checks of the E4M3 entry points (no CUDA call); *empty as check_args.
+int check_args_fp8(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
+                   int Nq, int Nk, int D, float scale, float q_descale, float k_descale, float v_descale,
+                   const void* workspace, size_t workspace_bytes, bool* empty) {
+  *empty = false;
+  if (!q || !k || !v || !o) return ATTN_EINVAL;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return ATTN_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_EINVAL;
+  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale) || q_descale <= 0.f ||
+      k_descale <= 0.f || v_descale <= 0.f)
+    return ATTN_EINVAL;
+  if (D != 128) return ATTN_EUNSUPPORTED;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_EUNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535) return ATTN_EUNSUPPORTED;
+  if (B == 0 || H == 0 || Nq == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  const size_t need = static_cast<size_t>(B) * H * D * ((static_cast<size_t>(Nk) + 15) / 16 * 16);
+  if (!workspace || workspace_bytes < need) return ATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_EUNSUPPORTED;
+  const int BH = B * H;
+  const size_t qb = static_cast<size_t>(BH) * Nq * D, kb = static_cast<size_t>(BH) * Nk * D;
+  const size_t ob = qb * 2, lb = static_cast<size_t>(BH) * Nq * 4;
+  if (ranges_overlap(o, ob, q, qb) || ranges_overlap(o, ob, k, kb) || ranges_overlap(o, ob, v, kb) ||
+      ranges_overlap(workspace, need, q, qb) || ranges_overlap(workspace, need, k, kb) ||
+      ranges_overlap(workspace, need, v, kb) || ranges_overlap(workspace, need, o, ob))
+    return ATTN_EUNSUPPORTED;
+  if (lse && (ranges_overlap(lse, lb, o, ob) || ranges_overlap(lse, lb, q, qb) || ranges_overlap(lse, lb, k, kb) ||
+              ranges_overlap(lse, lb, v, kb) || ranges_overlap(lse, lb, workspace, need)))
+    return ATTN_EUNSUPPORTED;
+  return ATTN_OK;
+}
+
+// Encodes the E4M3 forward's maps for heads [h0, h0 + nb) and enqueues the
+// V transpose and the forward on `st`.
+int enqueue_fp8(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, int h0, int nb,
+                int Nq, int Nk, float sl2, float v_descale, int causal, cudaStream_t st, uint64_t timeout, int drop) {
+  const int D = 128;
+  const int ldk = (Nk + 15) / 16 * 16;
+  const size_t qo = static_cast<size_t>(h0) * Nq * D, ko = static_cast<size_t>(h0) * Nk * D;
+  const size_t wo = static_cast<size_t>(h0) * D * ldk;
+  const uint8_t* qc = static_cast<const uint8_t*>(q) + qo;
+  const uint8_t* kc = static_cast<const uint8_t*>(k) + ko;
+  const uint8_t* vc = static_cast<const uint8_t*>(v) + ko;
+  uint8_t* wc = static_cast<uint8_t*>(workspace) + wo;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_u8(&mq, qc, nb, Nq, D, D) || !make_map_u8(&mk, kc, nb, Nk, D, D) ||
+      !make_map_u8(&mv, wc, nb, D, Nk, ldk))
+    return ATTN_ECUDA;
+  attn_fp8_transpose_v_kernel<<<dim3((Nk + 127) / 128, nb), 256, 0, st>>>(vc, wc, Nk, ldk);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ECUDA;
+  __half* oc = static_cast<__half*>(o) + qo;
+  float* lc = lse ? lse + static_cast<size_t>(h0) * Nq : nullptr;
+  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
+                                                             1, st, timeout, drop, v_descale)
+                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
+                                                              1, st, timeout, drop, v_descale);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1169,53 +1281,20 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
   int drop;
   debug_settings(&timeout, &drop);
   const float sl2 = scale * 1.4426950408889634f;
-  cudaStream_t user = static_cast<cudaStream_t>(stream);
-  std::lock_guard<std::mutex> lk(g_pipe_mu);
-  HostPipe* p = host_pipe(dev);
-  if (!p) return ATTN_ECUDA;
-  // Every internal stream starts after the work already queued on `user`
-  // (which may still use the device buffers), and `user` resumes when the
-  // last output has reached host memory.
-  if (cudaEventRecord(p->start, user) != cudaSuccess || cudaStreamWaitEvent(p->s_in, p->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->s_comp[0], p->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->s_comp[1], p->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(p->s_out, p->start, 0) != cudaSuccess)
-    return ATTN_ECUDA;
-  const auto H2D = cudaMemcpyHostToDevice;
-  const auto D2H = cudaMemcpyDeviceToHost;
-  for (int c = 0; c < chunks; ++c) {
-    // Chunks alternate between two compute streams, so that the next
-    // chunk's CTAs take the SMs the current one frees in its last wave.
-    cudaStream_t sc = p->s_comp[c & 1];
-    // heads [h0, h1) of the flattened B*H: contiguous in every tensor
-    const int h0 = static_cast<int>(static_cast<int64_t>(BH) * c / chunks);
-    const int h1 = static_cast<int>(static_cast<int64_t>(BH) * (c + 1) / chunks);
-    const int nb = h1 - h0;
-    const size_t qo = static_cast<size_t>(h0) * Nq * D * 2, ko = static_cast<size_t>(h0) * Nk * D * 2;
-    const size_t qn = static_cast<size_t>(nb) * Nq * D * 2, kn = static_cast<size_t>(nb) * Nk * D * 2;
-    const size_t lo = static_cast<size_t>(h0) * Nq, ln = static_cast<size_t>(nb) * Nq * 4;
-    auto at = [](const void* b, size_t off) { return static_cast<const char*>(b) + off; };
-    auto atw = [](void* b, size_t off) { return static_cast<char*>(b) + off; };
-    if (cudaMemcpyAsync(atw(q_dev, qo), at(q_host, qo), qn, H2D, p->s_in) != cudaSuccess ||
-        cudaMemcpyAsync(atw(k_dev, ko), at(k_host, ko), kn, H2D, p->s_in) != cudaSuccess ||
-        cudaMemcpyAsync(atw(v_dev, ko), at(v_host, ko), kn, H2D, p->s_in) != cudaSuccess ||
-        cudaEventRecord(p->in[c], p->s_in) != cudaSuccess || cudaStreamWaitEvent(sc, p->in[c], 0) != cudaSuccess)
-      return ATTN_ECUDA;
+  auto compute = [&](int, int h0, int nb, cudaStream_t sc) -> int {
+    const size_t qo = static_cast<size_t>(h0) * Nq * D, ko = static_cast<size_t>(h0) * Nk * D;
+    const __half* qc = static_cast<const __half*>(q_dev) + qo;
+    const __half* kc = static_cast<const __half*>(k_dev) + ko;
+    const __half* vc = static_cast<const __half*>(v_dev) + ko;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, at(q_dev, qo), nb, Nq, D) || !make_map(&mk, at(k_dev, ko), nb, Nk, D) ||
-        !make_map(&mv, at(v_dev, ko), nb, Nk, D))
+    if (!make_map(&mq, qc, nb, Nq, D) || !make_map(&mk, kc, nb, Nk, D) || !make_map(&mv, vc, nb, Nk, D))
       return ATTN_ECUDA;
-    const int r = dispatch_fwd<false>(D, causal, mq, mk, mv, atw(o_dev, qo), lse_dev ? lse_dev + lo : nullptr,
-                                      nullptr, nullptr, nb, Nq, Nk, sl2, 1, sc, timeout, drop);
-    if (r != ATTN_OK) return r;
-    if (cudaEventRecord(p->comp[c], sc) != cudaSuccess || cudaStreamWaitEvent(p->s_out, p->comp[c], 0) != cudaSuccess ||
-        cudaMemcpyAsync(atw(o_host, qo), at(o_dev, qo), qn, D2H, p->s_out) != cudaSuccess ||
-        (lse_host && cudaMemcpyAsync(lse_host + lo, lse_dev + lo, ln, D2H, p->s_out) != cudaSuccess))
-      return ATTN_ECUDA;
-  }
-  if (cudaEventRecord(p->done, p->s_out) != cudaSuccess || cudaStreamWaitEvent(user, p->done, 0) != cudaSuccess)
-    return ATTN_ECUDA;
-  return ATTN_OK;
+    return dispatch_fwd<false>(D, causal, mq, mk, mv, static_cast<__half*>(o_dev) + qo,
+                               lse_dev ? lse_dev + static_cast<size_t>(h0) * Nq : nullptr, nullptr, nullptr, nb, Nq,
+                               Nk, sl2, 1, sc, timeout, drop);
+  };
+  return host_pipeline(dev, q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev, BH, Nq,
+                       Nk, D, 2, chunks, static_cast<cudaStream_t>(stream), compute);
 }
 
 size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D) {
@@ -1226,50 +1305,51 @@ size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D) {
 int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
                  int D, float scale, int causal, float q_descale, float k_descale, float v_descale, void* workspace,
                  size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o) return ATTN_EINVAL;
-  if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return ATTN_EINVAL;
-  if (!std::isfinite(scale) || scale < 0.f) return ATTN_EINVAL;
-  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale) || q_descale <= 0.f ||
-      k_descale <= 0.f || v_descale <= 0.f)
-    return ATTN_EINVAL;
-  if (D != 128) return ATTN_EUNSUPPORTED;
-  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-  if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_EUNSUPPORTED;
-  if (static_cast<int64_t>(B) * H > 65535) return ATTN_EUNSUPPORTED;
-  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
-  const size_t need = attn_fp8_workspace_bytes(B, H, Nk, D);
-  if (!workspace || workspace_bytes < need) return ATTN_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_EUNSUPPORTED;
-  const int BH = B * H;
-  const size_t qb = static_cast<size_t>(BH) * Nq * D, kb = static_cast<size_t>(BH) * Nk * D;
-  const size_t ob = qb * 2, lb = static_cast<size_t>(BH) * Nq * 4;
-  if (ranges_overlap(o, ob, q, qb) || ranges_overlap(o, ob, k, kb) || ranges_overlap(o, ob, v, kb) ||
-      ranges_overlap(workspace, need, q, qb) || ranges_overlap(workspace, need, k, kb) ||
-      ranges_overlap(workspace, need, v, kb) || ranges_overlap(workspace, need, o, ob))
-    return ATTN_EUNSUPPORTED;
-  if (lse && (ranges_overlap(lse, lb, o, ob) || ranges_overlap(lse, lb, q, qb) || ranges_overlap(lse, lb, k, kb) ||
-              ranges_overlap(lse, lb, v, kb) || ranges_overlap(lse, lb, workspace, need)))
-    return ATTN_EUNSUPPORTED;
+  bool empty = false;
+  const int rc = check_args_fp8(q, k, v, o, lse, B, H, Nq, Nk, D, scale, q_descale, k_descale, v_descale, workspace,
+                                workspace_bytes, &empty);
+  if (rc != ATTN_OK || empty) return rc;
   const int sms = device_sms();
   if (sms <= 0) return -sms;
-  const int ldk = (Nk + 15) / 16 * 16;
-  CUtensorMap mq, mk, mv;
-  if (!make_map_u8(&mq, q, BH, Nq, D, D) || !make_map_u8(&mk, k, BH, Nk, D, D) ||
-      !make_map_u8(&mv, workspace, BH, D, Nk, ldk))
-    return ATTN_ECUDA;
   uint64_t timeout;
   int drop;
   debug_settings(&timeout, &drop);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  attn_fp8_transpose_v_kernel<<<dim3((Nk + 127) / 128, BH), 256, 0, st>>>(static_cast<const uint8_t*>(v),
-                                                                          static_cast<uint8_t*>(workspace), Nk, ldk);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ECUDA;
   const float sl2 = scale * q_descale * k_descale * 1.4426950408889634f;
-  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
-                                                                  sl2, 1, st, timeout, drop, v_descale)
-                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk,
-                                                                   sl2, 1, st, timeout, drop, v_descale);
+  return enqueue_fp8(q, k, v, o, lse, workspace, 0, B * H, Nq, Nk, sl2, v_descale, causal,
+                     static_cast<cudaStream_t>(stream), timeout, drop);
+}
+
+int attn_fwd_fp8_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                      void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int H, int Nq,
+                      int Nk, int D, float scale, int causal, float q_descale, float k_descale, float v_descale,
+                      void* workspace, size_t workspace_bytes, int num_chunks, void* stream) {
+  if (!q_host || !k_host || !v_host || !o_host) return ATTN_EINVAL;
+  if ((lse_host == nullptr) != (lse_dev == nullptr)) return ATTN_EINVAL;
+  if (num_chunks < 0 || num_chunks > kMaxHostChunks) return ATTN_EINVAL;
+  bool empty = false;
+  const int rc = check_args_fp8(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Nq, Nk, D, scale, q_descale, k_descale,
+                                v_descale, workspace, workspace_bytes, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  const int BH = B * H;
+  const size_t qb = static_cast<size_t>(BH) * Nq * D, kb = static_cast<size_t>(BH) * Nk * D;
+  if (ranges_overlap(q_dev, qb, k_dev, kb) || ranges_overlap(q_dev, qb, v_dev, kb) ||
+      ranges_overlap(k_dev, kb, v_dev, kb))
+    return ATTN_EUNSUPPORTED;  // the device copies of the inputs are written here
+  const int sms = device_sms();
+  if (sms <= 0) return -sms;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  const int chunks = std::max(1, std::min(num_chunks == 0 ? 32 : num_chunks, BH));
+  uint64_t timeout;
+  int drop;
+  debug_settings(&timeout, &drop);
+  const float sl2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  auto compute = [&](int, int h0, int nb, cudaStream_t sc) -> int {
+    return enqueue_fp8(q_dev, k_dev, v_dev, o_dev, lse_dev, workspace, h0, nb, Nq, Nk, sl2, v_descale, causal, sc,
+                       timeout, drop);
+  };
+  return host_pipeline(dev, q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev, BH, Nq,
+                       Nk, D, 1, chunks, static_cast<cudaStream_t>(stream), compute);
 }
 
 int attn_debug_pack_e4m3(const float* in, unsigned int* out, int n_quads, void* stream) {

@@ -357,10 +357,19 @@ def main():
         ho = torch.empty(o.shape, dtype=torch.float16).pin_memory()
         hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
 
-        host_entry = not fp8 and splits == 0
+        host_entry = splits == 0
 
         def e2e_step():
-            if host_entry:  # the library's host-buffer entry: copies overlapped with the forward
+            # the library's host-buffer entries: copies overlapped with the forward
+            if host_entry and fp8:
+                code = attn.attn_fwd_fp8_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(),
+                                              hl.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                              lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal,
+                                              1.0, 1.0, 1.0, ws.data_ptr(), ws.numel(), args.host_chunks, sptr)
+                if code != attn.ATTN_OK:
+                    raise attn.AttnError(code, "attn_fwd_fp8_host")
+                return
+            if host_entry:
                 code = attn.attn_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hl.data_ptr(),
                                           q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                           w.B, w.H, w.Nq, w.Nk, w.D, w.scale, w.causal, args.host_chunks, sptr)
@@ -388,7 +397,8 @@ def main():
         e_ms = multirank.max_over_ranks(e_ms, dist, dev)
         e2e = {"value": multirank.aggregate_tflops(f, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "steps": n_e2e,
-               "call": (f"attn_fwd_host, {args.host_chunks} head chunks, pinned host buffers" if host_entry
+               "call": (f"{'attn_fwd_fp8_host' if fp8 else 'attn_fwd_host'}, {args.host_chunks} head chunks, "
+                        f"pinned host buffers" if host_entry
                         else "copies in, forward, copies out on one stream, pinned host buffers"),
                "h2d_bytes_per_step": int(hq.numel() * hq.element_size() + hk.numel() * hk.element_size()
                                          + hv.numel() * hv.element_size()),

@@ -222,6 +222,20 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  int Nk, int D, float scale, int causal, float q_descale, float k_descale, float v_descale,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * attn_fwd_fp8_host -- attn_fwd_fp8 for tensors in HOST memory, pipelined
+ * over chunks of heads like attn_fwd_host (copies in, V transpose and
+ * forward, copies out, overlapped).  Host tensors: q_host, k_host, v_host in
+ * E4M3, o_host fp16, lse_host fp32 (may be NULL, then lse_dev too); device
+ * buffers of the full sizes and the workspace with attn_fwd_fp8's rules;
+ * num_chunks and stream as attn_fwd_host.  Errors as attn_fwd_fp8 and
+ * attn_fwd_host.
+ */
+int attn_fwd_fp8_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                      void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int H, int Nq,
+                      int Nk, int D, float scale, int causal, float q_descale, float k_descale, float v_descale,
+                      void* workspace, size_t workspace_bytes, int num_chunks, void* stream);
+
 /* Bytes of workspace attn_fwd_fp8 needs: B*H*D*round_up(Nk, 16).  0 for
  * negative sizes or D != 128. */
 size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D);

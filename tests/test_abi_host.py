@@ -173,3 +173,16 @@ def test_debug_pack_validation(lib):
 ])
 def test_host_entry_validation_without_device(lib, args, code):
     assert attn.attn_fwd_host(*args, None) == code
+
+
+def test_fp8_host_entry_validation_without_device(lib):
+    f = attn.attn_fwd_fp8_host
+    base = (W, W, W, W, None, A, A + (1 << 16), A + (2 << 16), 2 * A, None, 1, 1, 8, 8, 128, 0.1, 0, 1.0, 1.0, 1.0)
+    ws = (1 << 40, 1 << 20)
+    assert f(*((0,) + base[1:]), *ws, 0, None) == attn.ATTN_EINVAL                        # null host q
+    assert f(*(base[:4] + (W,) + base[5:]), *ws, 0, None) == attn.ATTN_EINVAL             # lse_host without lse_dev
+    assert f(*base, *ws, 65, None) == attn.ATTN_EINVAL                                   # too many chunks
+    assert f(*(base[:14] + (64,) + base[15:]), *ws, 0, None) == attn.ATTN_EUNSUPPORTED   # D = 64
+    assert f(*(base[:17] + (0.0,) + base[18:]), *ws, 0, None) == attn.ATTN_EINVAL        # q_descale 0
+    assert f(*(base[:6] + (A,) + base[7:]), *ws, 0, None) == attn.ATTN_EUNSUPPORTED      # k_dev = q_dev
+    assert f(*base, 0, 0, 0, None) == attn.ATTN_EINVAL                                   # no workspace

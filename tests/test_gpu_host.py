@@ -57,3 +57,30 @@ def test_host_entry_without_lse():
     torch.cuda.synchronize()
     assert attn.get_status() == attn.ATTN_OK
     assert torch.equal(oh, o1.cpu())
+
+
+@pytest.mark.parametrize("causal,chunks", [(False, 3), (True, 0)])
+def test_fp8_host_entry_equals_device_entry(causal, chunks):
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    B, H, Nq, Nk = 1, 5, 200, 300
+    q8, k8, v8 = synth.make_qkv_e4m3(B, H, Nq, Nk, 128, seed=5200 + chunks)
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q8, k8, v8))
+    qd, kd, vd = (torch.empty_like(x, device="cuda") for x in (qh, kh, vh))
+    od = torch.empty((B, H, Nq, 128), dtype=torch.float16, device="cuda")
+    ld = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(attn.fp8_workspace_bytes(B, H, Nk, 128), dtype=torch.uint8, device="cuda")
+    oh = torch.empty(od.shape, dtype=torch.float16).pin_memory()
+    lh = torch.empty(ld.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream().cuda_stream
+    code = attn.attn_fwd_fp8_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(), lh.data_ptr(),
+                                  qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
+                                  B, H, Nq, Nk, 128, 128 ** -0.5, causal, 0.5, 2.0, 1.5, ws.data_ptr(), ws.numel(),
+                                  chunks, stream)
+    assert code == attn.ATTN_OK
+    torch.cuda.synchronize()
+    o1, l1 = attn.fwd_fp8(*(torch.from_numpy(x).cuda() for x in (q8, k8, v8)), causal=causal,
+                          q_descale=0.5, k_descale=2.0, v_descale=1.5)
+    torch.cuda.synchronize()
+    assert attn.get_status() == attn.ATTN_OK
+    assert torch.equal(oh, o1.cpu()) and torch.equal(lh, l1.cpu())
