@@ -55,6 +55,31 @@ def read_peaks():
     return None, "fallback"
 
 
+def gpu_local_cpus(dev_index: int):
+    """The CPUs attached to the GPU's PCI root (sysfs local_cpulist), among
+    those this process may use; None when unknown.  On a Grace host the
+    pinned buffers of the end-to-end leg are first touched from these CPUs,
+    so that they sit in the memory of the GPU's own socket."""
+    import torch
+    p = torch.cuda.get_device_properties(dev_index)
+    ids = [getattr(p, a, None) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")]
+    if None in ids:
+        return None
+    dom, bus, dev = ids
+    for d in (f"{dom:04x}", f"{dom:08x}"):
+        path = f"/sys/bus/pci/devices/{d}:{bus:02x}:{dev:02x}.0/local_cpulist"
+        if not os.path.exists(path):
+            continue
+        cpus = set()
+        for part in open(path).read().strip().split(","):
+            if part:
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    return None
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     for rel in ("attention_forward_12_gb300/csrc/attn_fwd.cu",
@@ -353,9 +378,18 @@ def main():
     # ---------------- end to end: host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (qn, kn, vn))
-        ho = torch.empty(o.shape, dtype=torch.float16).pin_memory()
-        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        saved_affinity = os.sched_getaffinity(0)
+        local_cpus = gpu_local_cpus(local_rank)
+        if local_cpus:  # first touch of the pinned pages on the GPU's own socket
+            os.sched_setaffinity(0, local_cpus)
+        try:
+            hq, hk, hv = (torch.from_numpy(x).pin_memory() for x in (qn, kn, vn))
+            ho = torch.empty(o.shape, dtype=torch.float16).pin_memory()
+            hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+            ho.zero_()
+            hl.zero_()
+        finally:
+            os.sched_setaffinity(0, saved_affinity)
 
         host_entry = splits == 0
 
@@ -397,6 +431,8 @@ def main():
         e_ms = multirank.max_over_ranks(e_ms, dist, dev)
         e2e = {"value": multirank.aggregate_tflops(f, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "steps": n_e2e,
+               "host_buffers": (f"pinned, first touched on the {len(local_cpus)} CPUs local to the GPU"
+                                if local_cpus else "pinned (GPU-local CPUs unknown)"),
                "call": (f"{'attn_fwd_fp8_host' if fp8 else 'attn_fwd_host'}, {args.host_chunks} head chunks, "
                         f"pinned host buffers" if host_entry
                         else "copies in, forward, copies out on one stream, pinned host buffers"),
