@@ -62,6 +62,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -898,9 +899,19 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   using L = Layout<HD, NS, FP8>;
   auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
-      cudaSuccess)
-    return ATTN_ECUDA;
+  // The shared-memory attribute is set on the first launch on each device
+  // only: the host-buffer entry points launch once per chunk, and every
+  // driver call there is on the path that keeps the GPU fed.
+  static std::atomic<uint64_t> attr_set{0};  // one bit per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  const uint64_t bit = 1ull << dev;
+  if (!(attr_set.load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
+        cudaSuccess)
+      return ATTN_ECUDA;
+    attr_set.fetch_or(bit, std::memory_order_release);
+  }
   dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, splits);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
                                          o_scale, timeout_ns, drop);
