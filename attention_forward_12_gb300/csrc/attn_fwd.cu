@@ -915,6 +915,16 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, splits);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
                                          o_scale, timeout_ns, drop);
+  if (cudaGetLastError() == cudaSuccess) return ATTN_OK;
+  // A context reset (cudaDeviceReset) drops the attribute: set it again and
+  // retry once (a launch that failed did not run).
+  attr_set.fetch_and(~bit, std::memory_order_acq_rel);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
+      cudaSuccess)
+    return ATTN_ECUDA;
+  attr_set.fetch_or(bit, std::memory_order_release);
+  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
+                                         o_scale, timeout_ns, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
