@@ -27,11 +27,14 @@
 //     through shared memory).  Issue order per key tile j:
 //         O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
 //     so that one warpgroup's softmax runs while the tensor core works on
-//     the other's tile.  With SPLIT_P (the fp16 kernels) each O_w += P_w V_j
-//     is issued in two halves of 64 keys: the first as soon as the softmax
-//     has released the first half of P_w, overlapping the second half's
-//     exponentials -- this shortens each warpgroup's chain softmax -> P V ->
-//     Q K^T, which bounds the kernel.
+//     the other's tile.  With SPLIT_P (the fp16 D = 128 kernels) each
+//     O_w += P_w V_j is issued in two halves of 64 keys: the first as soon
+//     as the softmax has released the first half of P_w, overlapping the
+//     second half's exponentials -- this shortens each warpgroup's chain
+//     softmax -> P V -> Q K^T, which bounds the kernel.  At D = 64 the
+//     rotating score slots (below) already take S off that chain, and P is
+//     released whole: the second release and its wait cost more there than
+//     the overlap returns.
 //   * Softmax warpgroups w = 0, 1 (warps 4w..4w+3; thread t owns row t of
 //     query tile w, which is TMEM lane t): tcgen05.ld of S_w, mask, row
 //     maximum (3-input max), p = 2^(s*scale*log2(e) - m) with the scale
@@ -933,9 +936,9 @@ int dispatch_fwd(int D, int causal, const CUtensorMap& mq, const CUtensorMap& mk
                  void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
                  cudaStream_t st, uint64_t timeout, int drop) {
   if (D == 64)
-    return causal ? launch_fwd<64, true, 4, 2, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+    return causal ? launch_fwd<64, true, 4, 0, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
                                                                    splits, st, timeout, drop)
-                  : launch_fwd<64, false, 4, 2, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                  : launch_fwd<64, false, 4, 0, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                     sl2, splits, st, timeout, drop);
   return causal ? launch_fwd<128, true, 2, 2, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                     sl2, splits, st, timeout, drop)
