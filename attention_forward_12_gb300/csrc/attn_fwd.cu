@@ -39,11 +39,11 @@
 //     query tile w, which is TMEM lane t): tcgen05.ld of S_w, mask, row
 //     maximum (3-input max), p = 2^(s*scale*log2(e) - m) with the scale
 //     folded into a packed FFMA2, packed row sums, fp16 pack of p written
-//     back over S_w (in two released halves with SPLIT_P; SPLIT_P = 2 runs
-//     the O rescale between the halves, 1 before the exponentials).  O_w is
+//     back over S_w (in two released halves with SPLIT_P, the O rescale
+//     running between them; otherwise after the exponentials).  O_w is
 //     rescaled lazily, before the tile's P is released: only when a row's
-//     maximum grows
-//     by more than kTau (log2 units) over the reference it was using;
+//     maximum grows by more than kTau (log2 units) over the reference it
+//     was using;
 //     otherwise p is taken against the stale reference, which is exact
 //     because p, d and o share it (the conditional rescale the page credits
 //     to FlashAttention-4 in "Relationship to FA-3 and FA-4").  At the end the
@@ -202,6 +202,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 float sl2, float o_scale, uint64_t timeout_ns,
                 int drop_tile) {
   static_assert(!FP8 || HD == 128, "the E4M3 kernel is built for D = 128 only");
+  static_assert(SPLIT_P == 0 || SPLIT_P == 2, "P released whole (0) or in two halves (2)");
   using L = Layout<HD, NS, FP8>;
   constexpr uint32_t TB = L::kTileBytes;
 
@@ -508,62 +509,42 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const float2 sl2v = make_float2(sl2, sl2);
     float m_ref = -INFINITY;  // reference maximum, log2 units of the scaled score
     float dsum = 0.f;
-    // O_w must hold exactly P_0..P_{j-1} before it is rescaled and before
-    // P_j is released; every completion of O_w += P_w V is observed in order
-    // (in steady state it completed long ago).  The rescale itself is rare
-    // (lazy), except on sharply peaked rows whose maximum keeps growing.
-    auto rescale_o = [&](int j, bool resc, float alpha) -> bool {
-      if constexpr (SLOTS == 3) {
-        // With rotating slots this tile's scores may be ready before the
-        // previous tile's product is even issued, so the softmax waits for
-        // that product only when it must rescale.  Parity waits on the
-        // alternating barriers are exact: the product two before (j - 3)
-        // has completed -- the commit of this tile's S follows the issue
-        // of every product up to three items back -- and the one after
-        // (j + 1) cannot start before this tile's P is released.
-        if (!__any_sync(0xffffffffu, resc)) return true;
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[2 * wg + ((j - 1) & 1)], ((j - 1) >> 1) & 1, wc,
-                                               ATTN_ETIMEOUT)))
-          return false;
-      } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT))) return false;
-      }
+    // O_w *= alpha (the caller has found a row of the warp that rescales).
+    // O_w must hold exactly P_0..P_{j-1} first; completions of
+    // O_w += P_w V are observed in order.  With two slots the landing of
+    // S_j already implies that (its commit follows the issue of every
+    // earlier product), so the wait returns at once, and a tile that does
+    // not rescale does not wait at all.  With rotating slots this tile's
+    // scores may be ready before the previous tile's product is even
+    // issued; parity waits on the alternating barriers are exact: the
+    // product two before (j - 3) has completed -- the commit of this tile's
+    // S follows the issue of every product up to three items back -- and
+    // the one after (j + 1) cannot start before this tile's P is released.
+    // The rescale itself is rare (lazy), except on sharply peaked rows
+    // whose maximum keeps growing.  64 columns per TMEM round trip.
+    auto rescale_o = [&](int j, float alpha) -> bool {
+      const bool w_ok =
+          SLOTS == 3 ? mbar_wait(&o_done[2 * wg + ((j - 1) & 1)], ((j - 1) >> 1) & 1, wc, ATTN_ETIMEOUT)
+                     : mbar_wait(&o_done[wg], (j - 1) & 1, wc, ATTN_ETIMEOUT);
+      if (!__all_sync(0xffffffffu, w_ok)) return false;
       tc_fence_after();
-      if (__any_sync(0xffffffffu, resc)) {
-        const float2 al = make_float2(alpha, alpha);
-        if constexpr (SPLIT_P == 1) {
-          // Rescale runs before the exponentials, with the score row live:
-          // 8-column chunks keep it light on registers.
-#pragma unroll 1
-          for (int c = 0; c < HD / 8; ++c) {
-            uint32_t orr[8];
-            tmem_ld8(tO + c * 8, orr);
-            tmem_ld_wait8(orr);
+      const float2 al = make_float2(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
-              orr[e] = __float_as_uint(v.x);
-              orr[e + 1] = __float_as_uint(v.y);
-            }
-            tmem_st8(tO + c * 8, orr);
+      for (int c = 0; c < HD / 32; c += 2) {
+        uint32_t o2[2][32];
+        tmem_ld32(tO + c * 32, o2[0]);
+        tmem_ld32(tO + (c + 1) * 32, o2[1]);
+        tmem_ld_wait(o2[0]);
+        tmem_ld_wait(o2[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o2[h][e]), __uint_as_float(o2[h][e + 1])), al);
+            o2[h][e] = __float_as_uint(v.x);
+            o2[h][e + 1] = __float_as_uint(v.y);
           }
-        } else {
-          // Rescale runs after the exponentials (the score row is dead), or
-          // between the two halves of P (half of it live): full 32-column
-          // chunks, unrolled.
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(tO + c * 32, orr);
-            tmem_ld_wait(orr);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al);
-              orr[e] = __float_as_uint(v.x);
-              orr[e + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(tO + c * 32, orr);
-          }
+          tmem_st32(tO + (c + h) * 32, o2[h]);
         }
       }
       return true;
@@ -612,13 +593,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         m_ref = mt;
         dsum *= alpha;
       }
-      if constexpr (SPLIT_P == 1) {
-        if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
-      }
       bool mid_ok = true;
       auto mid = [&]() {
         if constexpr (SPLIT_P == 2) {
-          if (j >= 1) mid_ok = rescale_o(j, resc, alpha);
+          // Between the halves the first half's scores are dead and the
+          // second half's are still in TMEM (P covers columns [0, 64) of
+          // the slot): a rescaling warp drops them from registers for the
+          // rescale and loads them back.
+          if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+            mid_ok = rescale_o(j, alpha);
+            if (mid_ok) {
+              tmem_ld32(tS + 64, sr[2]);
+              tmem_ld32(tS + 96, sr[3]);
+              tmem_ld_wait(sr[2]);
+              tmem_ld_wait(sr[3]);
+              if (masked) {
+#pragma unroll
+                for (int c = 2; c < 4; ++c)
+#pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+              }
+            }
+          }
         }
       };
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
@@ -636,7 +633,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (!(ok = mid_ok)) break;
       if constexpr (!SPLIT_P) {
-        if (j >= 1 && !(ok = rescale_o(j, resc, alpha))) break;
+        if (j >= 1 && __any_sync(0xffffffffu, resc) && !(ok = rescale_o(j, alpha))) break;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[slot]);
