@@ -129,8 +129,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // to the MMA thread as soon as it is in TMEM, `mid` running just before the
 // first release.  Returns the row sum of the fp32 p.  MASK: 0 = columns
 // >= lim masked when `masked` (decided at run time), 1 = none masked, 2 =
-// columns >= lim masked.
-template <int MASK, int EMU, int SPLIT_P, bool FP8, typename Mid>
+// columns >= lim masked.  EARLY (fp16): each 32 keys of P go to TMEM as soon
+// as they are packed, instead of one store per half.
+template <int MASK, int EMU, int SPLIT_P, bool FP8, bool EARLY, typename Mid>
 __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2v, float2 nm, bool masked, int lim,
                                          uint32_t tS, uint64_t* p_half, uint64_t* p_full, Mid&& mid) {
   const bool mk = MASK == 2 || (MASK == 0 && masked);
@@ -138,6 +139,7 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t pk[FP8 ? 16 : 32];
+    uint32_t pq[2][16];
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * h + cc;
@@ -164,15 +166,19 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
         }
         if constexpr (FP8) {
           pk[cc * 8 + (e >> 2)] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
+        } else if constexpr (EARLY) {
+          pq[cc][e >> 1] = pack_half2(p[0], p[1]);
+          pq[cc][(e >> 1) + 1] = pack_half2(p[2], p[3]);
         } else {
           pk[cc * 16 + (e >> 1)] = pack_half2(p[0], p[1]);
           pk[cc * 16 + (e >> 1) + 1] = pack_half2(p[2], p[3]);
         }
       }
+      if constexpr (!FP8 && EARLY) tmem_st16(tS + h * 32 + cc * 16, pq[cc]);
     }
     if constexpr (FP8) {
       tmem_st16(tS + h * 16, pk);
-    } else {
+    } else if constexpr (!EARLY) {
       tmem_st32(tS + h * 32, pk);
     }
     if constexpr (SPLIT_P) {
@@ -626,10 +632,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // was measured to pay (causal, D = 64); the non-causal D = 128 kernel
       // keeps one loop with the mask decided at run time.
       if constexpr (CAUSAL || HD == 64) {
-        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8>(sr, sl2v, nm, true, lim, tS, &p_half[slot], &p_full[slot], mid)
-                       : exp_row<1, EMU, SPLIT_P, FP8>(sr, sl2v, nm, false, lim, tS, &p_half[slot], &p_full[slot], mid);
+        dsum += masked ? exp_row<2, EMU, SPLIT_P, FP8, HD == 64>(sr, sl2v, nm, true, lim, tS, &p_half[slot], &p_full[slot], mid)
+                       : exp_row<1, EMU, SPLIT_P, FP8, HD == 64>(sr, sl2v, nm, false, lim, tS, &p_half[slot], &p_full[slot], mid);
       } else {
-        dsum += exp_row<0, EMU, SPLIT_P, FP8>(sr, sl2v, nm, masked, lim, tS, &p_half[slot], &p_full[slot], mid);
+        dsum += exp_row<0, EMU, SPLIT_P, FP8, HD == 64>(sr, sl2v, nm, masked, lim, tS, &p_half[slot], &p_full[slot], mid);
       }
       if (!(ok = mid_ok)) break;
       if constexpr (!SPLIT_P) {
