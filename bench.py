@@ -417,9 +417,9 @@ def main():
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
-        # The box's pinned host-to-device bandwidth, for reading the end-to-end
-        # figure: the forward hides its input copies only while they run faster
-        # than it consumes them.
+        # The box's pinned host-to-device and device-to-host bandwidths, for
+        # reading the end-to-end figure: the forward hides its copies only
+        # while they run faster than it consumes and produces the data.
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         q.copy_(hq, non_blocking=True)
         a.record(stream)
@@ -427,6 +427,11 @@ def main():
         b.record(stream)
         b.synchronize()
         h2d_gbs = hq.numel() * hq.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+        a.record(stream)
+        ho.copy_(o, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        d2h_gbs = ho.numel() * ho.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
         n_e2e = max(3, min(args.steps, 10))
         for _ in range(2):
             e2e_step()
@@ -442,6 +447,7 @@ def main():
         e2e = {"value": multirank.aggregate_tflops(f, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "steps": n_e2e,
                "h2d_gbs_measured": h2d_gbs,
+               "d2h_gbs_measured": d2h_gbs,
                "host_buffers": (f"pinned, first touched on the {len(local_cpus)} CPUs local to the GPU"
                                 if local_cpus else "pinned (GPU-local CPUs unknown)"),
                "call": (f"{'attn_fwd_fp8_host' if fp8 else 'attn_fwd_host'}, {args.host_chunks} head chunks, "
