@@ -36,8 +36,9 @@
 //     released whole: the second release and its wait cost more there than
 //     the overlap returns.
 //   * Softmax warpgroups w = 0, 1 (warps 4w..4w+3; thread t owns row t of
-//     query tile w, which is TMEM lane t): tcgen05.ld of S_w, mask, row
-//     maximum (3-input max), p = 2^(s*scale*log2(e) - m) with the scale
+//     query tile w, which is TMEM lane t): tcgen05.ld.red of S_w, which
+//     returns the row maximum with the scores (masked tiles: mask, then a
+//     3-input max pass), p = 2^(s*scale*log2(e) - m) with the scale
 //     folded into a packed FFMA2, packed row sums, fp16 pack of p written
 //     back over S_w (in two released halves with SPLIT_P, the O rescale
 //     running between them; otherwise after the exponentials).  O_w is
@@ -566,31 +567,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], par, wc, ATTN_ETIMEOUT));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-
       const int key0 = (t0 + j) * kBlockN;
       const bool masked = (key0 + kBlockN > Nk) || (CAUSAL && key0 + kBlockN - 1 > rw);
       const int lim = row_lim - key0;  // columns [0, lim) of this tile are admissible
+      // The reducing TMEM load hands back each row's maximum with its
+      // scores, so unmasked tiles need no maximum pass over the registers.
+      // Masked columns must not enter the maximum: masked tiles (the
+      // diagonal, the ragged last tile) mask and take a 3-input max pass.
+      uint32_t sr[4][32];
+      float m4[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + c * 32, sr[c], m4[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait_max(sr[c], m4[c]);
+      float mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+              mx4[a] = max3(mx4[a], __uint_as_float(sr[c][e + 2 * a]), __uint_as_float(sr[c][e + 2 * a + 1]));
+        mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
       }
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 8)
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-            mx4[a] = max3(mx4[a], __uint_as_float(sr[c][e + 2 * a]), __uint_as_float(sr[c][e + 2 * a + 1]));
-      const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
       const float mt = (mx == -INFINITY) ? -INFINITY : mx * sl2;
       const bool resc = mt > m_ref + kTau;
       float alpha = 1.f;
