@@ -13,13 +13,15 @@ import threading
 
 from ._build import LIB_PATH
 
-ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_ESCRATCH = 0, 1, 2, 3, 4, 5
+ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_ESCRATCH, ATTN_ETOOLONG = range(7)
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+MAX_KEYS_PER_PASS = 1 << 19
 
 # Every symbol the C header declares; the CPU tests check they are exported.
 EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
            "attn_fwd_splitkv_noalloc", "attn_fwd_fp8", "attn_fwd_fp8_host", "attn_fp8_workspace_bytes", "attn_debug_pack_e4m3",
-           "attn_strerror", "attn_get_status", "attn_debug_set", "attn_version")
+           "attn_debug_exp2_poly", "attn_debug_fwd_poly_exp", "attn_strerror", "attn_get_status", "attn_debug_set",
+           "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +66,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32]
             lib.attn_debug_pack_e4m3.restype = i32
             lib.attn_debug_pack_e4m3.argtypes = [vp, vp, i32, vp]
+            lib.attn_debug_exp2_poly.restype = i32
+            lib.attn_debug_exp2_poly.argtypes = [vp, vp, i32, vp]
+            lib.attn_debug_fwd_poly_exp.restype = i32
+            lib.attn_debug_fwd_poly_exp.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                    ctypes.c_float, i32, vp]
             lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.attn_splitkv_suggest.restype = i32
@@ -159,7 +166,7 @@ def _current_stream_ptr(device) -> int:
 
 
 def fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse=None,
-        want_lse: bool = True):
+        want_lse: bool = True, _entry=None):
     """O = softmax(scale * Q K^T) V on the GPU; returns (o, lse).
 
     q: fp16 CUDA tensor [B,H,Nq,D], k and v: [B,H,Nk,D], contiguous.
@@ -182,12 +189,28 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse
         out = torch.empty_like(q)
     if want_lse and lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    code = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                    lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, D, scale, causal,
-                    _current_stream_ptr(q.device))
+    entry = attn_fwd if _entry is None else _entry
+    code = entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                 lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, D, scale, causal,
+                 _current_stream_ptr(q.device))
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd")
     return out, lse
+
+
+def attn_debug_fwd_poly_exp(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None,
+                            B: int, H: int, Nq: int, Nk: int, D: int, scale: float, causal: bool,
+                            stream: int | None) -> int:
+    """The testing hook that runs attn_fwd with a quarter of the exponentials
+    on the FMA-pipe polynomial (raw device pointers; returns the code)."""
+    return load_library().attn_debug_fwd_poly_exp(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
+                                                  int(Nq), int(Nk), int(D), float(scale),
+                                                  int(bool(causal)), stream)
+
+
+def fwd_poly_exp(q, k, v, scale: float | None = None, causal: bool = False):
+    """fwd through the polynomial-exponential testing hook; returns (o, lse)."""
+    return fwd(q, k, v, scale=scale, causal=causal, _entry=attn_debug_fwd_poly_exp)
 
 
 def fwd_host(q, k, v, scale: float | None = None, causal: bool = False, num_chunks: int = 0,
@@ -317,6 +340,20 @@ def debug_pack_e4m3(x):
     if code != ATTN_OK:
         raise AttnError(code, "attn_debug_pack_e4m3")
     return out.view(torch.uint8)
+
+
+def debug_exp2_poly(x):
+    """2^x by the forward's FMA-pipe polynomial, for a contiguous float32
+    CUDA tensor; returns a new tensor."""
+    import torch
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous CUDA float32 tensor")
+    out = torch.empty_like(x)
+    code = load_library().attn_debug_exp2_poly(x.data_ptr(), out.data_ptr(), x.numel(),
+                                               _current_stream_ptr(x.device))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_debug_exp2_poly")
+    return out
 
 
 def get_status(stream: int | None = None) -> int:

@@ -92,6 +92,9 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // Exponentials sent to the FMA-pipe polynomial: one pair in kEmu (0 = none).
 constexpr int kEmu64 = 0;
 constexpr int kEmu128 = 0;
+// The share attn_debug_fwd_poly_exp sends there (one pair in four), so that
+// the polynomial's device code runs inside the forward under test.
+constexpr int kDebugEmu = 4;
 
 template <int HD, int NS, bool FP8 = false>
 struct Layout {
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
                 float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_l, int Nq, int Nk,
-                float sl2, float o_scale, uint64_t timeout_ns,
+                float sl2, float o_scale, int* status_host, uint64_t timeout_ns,
                 int drop_tile) {
   static_assert(!FP8 || HD == 128, "the E4M3 kernel is built for D = 128 only");
   static_assert(SPLIT_P == 0 || SPLIT_P == 2, "P released whole (0) or in two halves (2)");
@@ -320,7 +323,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int mmin = min(nkv0, nkv1);
   const int wlong = nkv0 > nkv1 ? 0 : 1;
   const int nitems = nkv0 + nkv1;
-  const WaitCtl wc{abort_flag, &g_attn_status, timeout_ns};
+  const WaitCtl wc{abort_flag, &g_attn_status, status_host, timeout_ns};
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -755,6 +758,9 @@ attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restric
   const size_t row = static_cast<size_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  // Like the forward, no work while the status word holds an error: the
+  // parts of a forward that stopped early were never written.
+  if (*static_cast<volatile int*>(&g_attn_status) != 0) return;
   float m = -INFINITY;
   for (int s = 0; s < splits; ++s) m = fmaxf(m, ws_l[static_cast<size_t>(s) * rows + row]);
   float acc[kPer];
@@ -841,6 +847,16 @@ __global__ void attn_debug_pack_e4m3_kernel(const float* __restrict__ in, uint32
   if (i < n) out[i] = pack_e4m3x4(in[4 * i], in[4 * i + 1], in[4 * i + 2], in[4 * i + 3]);
 }
 
+// 2^x on the FMA pipe (exp2_poly2) on its own, for tests: out[i] = 2^in[i].
+__global__ void attn_debug_exp2_poly_kernel(const float* __restrict__ in, float* __restrict__ out, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float2 x = make_float2(in[i], i + 1 < n ? in[i + 1] : in[i]);
+  const float2 y = exp2_poly2(x);
+  out[i] = y.x;
+  if (i + 1 < n) out[i + 1] = y.y;
+}
+
 // =====================================================================
 // Host side
 // =====================================================================
@@ -849,24 +865,32 @@ namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
 std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
 int g_drop_tile = -1;
 constexpr int kMaxDevices = 64;
-int g_dev_ready[kMaxDevices];  // 1 = attributes set and device checked; -1 = unsupported
+
+// A driver entry point, looked up through the runtime (so that the library
+// loads on a machine without a driver).  Call with g_mu held.
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(fn);
+}
 
 EncodeTiledFn encode_fn() {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-  }
+  if (!g_encode) g_encode = driver_fn<EncodeTiledFn>("cuTensorMapEncodeTiled");
   return g_encode;
 }
 
@@ -904,10 +928,132 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// ------------------------------------------------------------ device state
+// Built-in scratch of attn_fwd_splitkv_noalloc: holds the split-KV parts for
+// callers that cannot allocate device memory.  Every device that loads the
+// library carries it until the process exits.  In host code the name below
+// only stands in for the buffer; its device address comes from
+// cudaGetSymbolAddress, looked up with the device current (ContextState).
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// What the library keeps per CUDA context: the sm_103 check and SM count,
+// the host copy of the device status word (page-locked host memory mapped
+// into the device: kernels write it when a wait runs out, and the entry
+// points read it before enqueueing anything), and the device address of the
+// no-allocation scratch.  Entries are keyed by the context's unique id: a
+// context reset (cudaDeviceReset) makes a new context, whose first call
+// sets up a new entry, while the old entry's memory went with the old
+// context.  Created on the first call in a context and never freed.
+struct ContextState {
+  unsigned long long ctx_id = 0;
+  int sms = 0;                    // > 0, or 0 when the device is not an sm_103 part
+  int* status_host = nullptr;     // host view of the copy (null if it could not be made)
+  int* status_dev = nullptr;      // device view of the same word
+  void* noalloc = nullptr;        // device address of g_noalloc_scratch (looked up on first use)
+};
+constexpr int kMaxContexts = 64;
+ContextState g_ctx[kMaxContexts];
+int g_nctx = 0;
+
+// Unique id of the calling thread's current context (made current by the
+// runtime if none is).  Call with g_mu held.
+bool current_ctx_id(unsigned long long* id) {
+  if (!g_ctx_current) g_ctx_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  if (!g_ctx_id) g_ctx_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  if (ctx == nullptr) {  // the runtime has not bound its primary context to this thread yet
+    if (cudaFree(nullptr) != cudaSuccess || g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  }
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// The current context's entry, created on first use; call with g_mu held.
+// Returns ATTN_OK, ATTN_EUNSUPPORTED (not an sm_103 part) or ATTN_ECUDA.
+int context_state(ContextState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  unsigned long long id = 0;
+  if (!current_ctx_id(&id)) return ATTN_ECUDA;
+  ContextState* st = nullptr;
+  for (int i = 0; i < g_nctx && !st; ++i)
+    if (g_ctx[i].ctx_id == id) st = &g_ctx[i];
+  if (!st) {
+    ContextState fresh;
+    fresh.ctx_id = id;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_ECUDA;
+    fresh.sms = (prop.major == 10 && prop.minor == 3) ? prop.multiProcessorCount : 0;
+    if (fresh.sms > 0) {
+      int* h = nullptr;
+      void* d = nullptr;
+      if (cudaHostAlloc(reinterpret_cast<void**>(&h), sizeof(int), cudaHostAllocMapped | cudaHostAllocPortable) ==
+          cudaSuccess) {
+        if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
+          *h = 0;
+          fresh.status_host = h;
+          fresh.status_dev = static_cast<int*>(d);
+        } else {
+          cudaFreeHost(h);
+        }
+      }
+      cudaGetLastError();  // a failed optional step leaves no sticky runtime error behind
+    }
+    if (g_nctx == kMaxContexts) {  // table full (many contexts): serve without caching
+      static thread_local ContextState spare;
+      spare = fresh;
+      st = &spare;
+    } else {
+      g_ctx[g_nctx] = fresh;
+      st = &g_ctx[g_nctx++];
+    }
+  }
+  if (st->sms <= 0) return ATTN_EUNSUPPORTED;
+  *out = st;
+  return ATTN_OK;
+}
+
+// What every launch takes besides its tensors: the host copy of the status
+// word and the testing hook's settings.
+struct RunCtl {
+  int* status_dev = nullptr;
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  int drop = -1;
+  int sms = 0;
+  void* noalloc = nullptr;
+};
+
+// Entry of every forward call (after its argument checks): the current
+// context's state and the testing hook's settings.  Returns ATTN_ETIMEOUT,
+// without touching the device, while the host copy of the status word holds
+// an error that attn_get_status() has not yet cleared.  want_noalloc also
+// looks up the no-allocation scratch (once per context).
+int enter(RunCtl* rc, bool want_noalloc = false) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  ContextState* st = nullptr;
+  const int r = context_state(&st);
+  if (r != ATTN_OK) return r;
+  if (st->status_host != nullptr && *static_cast<volatile int*>(st->status_host) != 0) return ATTN_ETIMEOUT;
+  if (want_noalloc && st->noalloc == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ECUDA;
+    st->noalloc = ptr;
+  }
+  rc->status_dev = st->status_dev;
+  rc->timeout_ns = g_timeout_ns;
+  rc->drop = g_drop_tile;
+  rc->sms = st->sms;
+  rc->noalloc = st->noalloc;
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------ launches
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
                float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
-               uint64_t timeout_ns, int drop, float o_scale = 1.0f) {
+               const RunCtl& rc, float o_scale = 1.0f) {
   using L = Layout<HD, NS, FP8>;
   auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
@@ -926,7 +1072,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   }
   dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, splits);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         o_scale, timeout_ns, drop);
+                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop);
   if (cudaGetLastError() == cudaSuccess) return ATTN_OK;
   // A context reset (cudaDeviceReset) drops the attribute: set it again and
   // retry once (a launch that failed did not run).
@@ -936,23 +1082,26 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     return ATTN_ECUDA;
   attr_set.fetch_or(bit, std::memory_order_release);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         o_scale, timeout_ns, drop);
+                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
-template <bool SPLITKV>
+// The fp16 forward: D = 64 with three rotating score slots and P released
+// whole, D = 128 with P released in two halves.  EMU: one pair of
+// exponentials in EMU on the FMA-pipe polynomial (0 = none).
+template <bool SPLITKV, int EMU64 = kEmu64, int EMU128 = kEmu128>
 int dispatch_fwd(int D, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                  void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
-                 cudaStream_t st, uint64_t timeout, int drop) {
+                 cudaStream_t st, const RunCtl& rc) {
   if (D == 64)
-    return causal ? launch_fwd<64, true, 4, 0, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
-                                                                   splits, st, timeout, drop)
-                  : launch_fwd<64, false, 4, 0, kEmu64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
-                                                                    sl2, splits, st, timeout, drop);
-  return causal ? launch_fwd<128, true, 2, 2, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
-                                                                    sl2, splits, st, timeout, drop)
-                : launch_fwd<128, false, 2, 2, kEmu128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
-                                                                     sl2, splits, st, timeout, drop);
+    return causal ? launch_fwd<64, true, 4, 0, EMU64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                                                                         sl2, splits, st, rc)
+                  : launch_fwd<64, false, 4, 0, EMU64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                                                                          sl2, splits, st, rc);
+  return causal ? launch_fwd<128, true, 2, 2, EMU128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+                                                               splits, st, rc)
+                : launch_fwd<128, false, 2, 2, EMU128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+                                                                splits, st, rc);
 }
 
 // Argument checks shared by the forward entry points (no CUDA call).
@@ -984,23 +1133,23 @@ int check_args(const void* q, const void* k, const void* v, const void* o, const
   return ATTN_OK;
 }
 
-// The current device must be an sm_103 part; returns its SM count or <= 0.
-int device_sms() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -ATTN_ECUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_dev_ready[dev] == 0) {
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return -ATTN_ECUDA;
-    g_dev_ready[dev] = (prop.major == 10 && prop.minor == 3) ? prop.multiProcessorCount : -1;
-  }
-  return g_dev_ready[dev] > 0 ? g_dev_ready[dev] : -ATTN_EUNSUPPORTED;
+// Key tiles of the longest query-tile pair (the kernel's nkv for the pair
+// with the most admissible keys).
+int64_t pair_key_tiles(int Nq, int Nk, int causal) {
+  const int64_t pairs_end = (static_cast<int64_t>(Nq) + kRowsPerCta - 1) / kRowsPerCta * kRowsPerCta;
+  const int64_t keys = causal ? std::min<int64_t>(Nk, pairs_end) : Nk;
+  return (keys + kBlockN - 1) / kBlockN;
 }
 
-void debug_settings(uint64_t* timeout, int* drop) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  *timeout = g_timeout_ns;
-  *drop = g_drop_tile;
+// ATTN_ETOOLONG when a row would accumulate more than ATTN_MAX_KEYS_PER_PASS
+// keys in one pass (one share of `splits`); 0 = the single-pass forward.
+int check_keys_per_pass(int Nq, int Nk, int causal, int splits) {
+  if (splits == 0) {
+    const int64_t keys = causal ? std::min(Nk, Nq) : Nk;
+    return keys > ATTN_MAX_KEYS_PER_PASS ? ATTN_ETOOLONG : ATTN_OK;
+  }
+  const int64_t share_tiles = (pair_key_tiles(Nq, Nk, causal) + splits - 1) / splits;
+  return share_tiles * kBlockN > ATTN_MAX_KEYS_PER_PASS ? ATTN_ETOOLONG : ATTN_OK;
 }
 
 constexpr int kMaxSplits = 256;
@@ -1019,25 +1168,21 @@ int launch_merge(const float* ws_o, const float* ws_l, void* o, float* lse, size
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
-// Built-in scratch of attn_fwd_splitkv_noalloc: holds the split-KV parts for
-// callers that cannot allocate device memory.  Every device that loads the
-// library carries it until the process exits.  In host code the name below
-// only stands in for the buffer; its device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
-constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES);
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
-
-void* noalloc_scratch_address(int dev) {
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
-    g_noalloc_addr[dev] = ptr;
-  }
-  return g_noalloc_addr[dev];
+// The split-KV forward and its merge on `workspace` (parts, then the
+// per-row log-sum-exps), once the arguments have been checked.
+int enqueue_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Nq, int Nk, int D,
+                    float scale, int causal, int num_splits, void* workspace, cudaStream_t st, const RunCtl& rc) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
+    return ATTN_ECUDA;
+  const float sl2 = scale * 1.4426950408889634f;
+  const size_t rows = static_cast<size_t>(BH) * Nq;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_l = ws_o + static_cast<size_t>(num_splits) * rows * D;
+  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st, rc);
+  if (r != ATTN_OK) return r;
+  return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
+                 : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
 }
 
 // Streams and events of attn_fwd_host, created once per device on first
@@ -1158,7 +1303,7 @@ int check_args_fp8(const void* q, const void* k, const void* v, const void* o, c
 // Encodes the E4M3 forward's maps for heads [h0, h0 + nb) and enqueues the
 // V transpose and the forward on `st`.
 int enqueue_fp8(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, int h0, int nb,
-                int Nq, int Nk, float sl2, float v_descale, int causal, cudaStream_t st, uint64_t timeout, int drop) {
+                int Nq, int Nk, float sl2, float v_descale, int causal, cudaStream_t st, const RunCtl& rc) {
   const int D = 128;
   const int ldk = (Nk + 15) / 16 * 16;
   const size_t qo = static_cast<size_t>(h0) * Nq * D, ko = static_cast<size_t>(h0) * Nk * D;
@@ -1176,9 +1321,21 @@ int enqueue_fp8(const void* q, const void* k, const void* v, void* o, float* lse
   __half* oc = static_cast<__half*>(o) + qo;
   float* lc = lse ? lse + static_cast<size_t>(h0) * Nq : nullptr;
   return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
-                                                             1, st, timeout, drop, v_descale)
+                                                             1, st, rc, v_descale)
                 : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
-                                                              1, st, timeout, drop, v_descale);
+                                                              1, st, rc, v_descale);
+}
+
+// The single-pass fp16 forward, once the arguments have been checked.
+template <int EMU64 = kEmu64, int EMU128 = kEmu128>
+int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Nq, int Nk, int D,
+                float scale, int causal, cudaStream_t st, const RunCtl& rc) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
+    return ATTN_ECUDA;
+  const float sl2 = scale * 1.4426950408889634f;
+  return dispatch_fwd<false, EMU64, EMU128>(D, causal, mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk, sl2, 1, st,
+                                            rc);
 }
 
 }  // namespace
@@ -1188,20 +1345,12 @@ extern "C" {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
              int D, float scale, int causal, void* stream) {
   bool empty = false;
-  const int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
   if (rc != ATTN_OK || empty) return rc;
-  const int sms = device_sms();
-  if (sms <= 0) return -sms;
-  const int BH = B * H;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
-    return ATTN_ECUDA;
-  uint64_t timeout;
-  int drop;
-  debug_settings(&timeout, &drop);
-  const float sl2 = scale * 1.4426950408889634f;
-  return dispatch_fwd<false>(D, causal, mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk, sl2, 1,
-                             static_cast<cudaStream_t>(stream), timeout, drop);
+  if ((rc = check_keys_per_pass(Nq, Nk, causal, 0)) != ATTN_OK) return rc;
+  RunCtl run;
+  if ((rc = enter(&run)) != ATTN_OK) return rc;
+  return enqueue_fwd(q, k, v, o, lse, B * H, Nq, Nk, D, scale, causal, static_cast<cudaStream_t>(stream), run);
 }
 
 size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits) {
@@ -1211,13 +1360,19 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits)
 
 int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (D != 64 && D != 128)) return 0;
-  const int sms = device_sms();
-  if (sms <= 0) return 0;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    ContextState* st = nullptr;
+    if (context_state(&st) != ATTN_OK) return 0;
+    sms = st->sms;
+  }
   const int64_t ctas = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
-  const int key_tiles = (causal ? std::min(Nk, kRowsPerCta * ((Nq + kRowsPerCta - 1) / kRowsPerCta)) : Nk);
-  const int tiles = (key_tiles + kBlockN - 1) / kBlockN;
-  int64_t s = (sms + ctas - 1) / ctas;             // fill the SMs once
-  s = std::min<int64_t>(s, std::max(1, tiles / 4));  // at least 4 key tiles per share
+  const int64_t tiles = pair_key_tiles(Nq, Nk, causal);
+  int64_t s = (sms + ctas - 1) / ctas;               // fill the SMs once
+  s = std::min<int64_t>(s, std::max<int64_t>(1, tiles / 4));  // at least 4 key tiles per share
+  // no share longer than one pass may accumulate
+  s = std::max<int64_t>(s, (tiles * kBlockN + ATTN_MAX_KEYS_PER_PASS - 1) / ATTN_MAX_KEYS_PER_PASS);
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits)));
 }
 
@@ -1225,7 +1380,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      int Nk, int D, float scale, int causal, int num_splits, void* workspace,
                      size_t workspace_bytes, void* stream) {
   bool empty = false;
-  const int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
   if (rc != ATTN_OK) return rc;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_EINVAL;
   if (empty) return ATTN_OK;
@@ -1238,57 +1393,26 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
       ranges_overlap(workspace, need, v, kvbytes) || ranges_overlap(workspace, need, o, qbytes) ||
       (lse && ranges_overlap(workspace, need, lse, static_cast<size_t>(BH) * Nq * 4)))
     return ATTN_EUNSUPPORTED;
-  const int sms = device_sms();
-  if (sms <= 0) return -sms;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
-    return ATTN_ECUDA;
-  uint64_t timeout;
-  int drop;
-  debug_settings(&timeout, &drop);
-  const float sl2 = scale * 1.4426950408889634f;
-  const size_t rows = static_cast<size_t>(BH) * Nq;
-  float* ws_o = static_cast<float*>(workspace);
-  float* ws_l = ws_o + static_cast<size_t>(num_splits) * rows * D;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st,
-                                   timeout, drop);
-  if (r != ATTN_OK) return r;
-  return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
-                 : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
+  if ((rc = check_keys_per_pass(Nq, Nk, causal, num_splits)) != ATTN_OK) return rc;
+  RunCtl run;
+  if ((rc = enter(&run)) != ATTN_OK) return rc;
+  return enqueue_splitkv(q, k, v, o, lse, BH, Nq, Nk, D, scale, causal, num_splits, workspace,
+                         static_cast<cudaStream_t>(stream), run);
 }
 
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                              int Nq, int Nk, int D, float scale, int causal, int num_splits, void* stream) {
   bool empty = false;
-  const int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
   if (rc != ATTN_OK) return rc;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_EINVAL;
   if (empty) return ATTN_OK;
   if (splitkv_bytes(B, H, Nq, D, num_splits) > kNoAllocScratchBytes) return ATTN_ESCRATCH;
-  const int sms = device_sms();
-  if (sms <= 0) return -sms;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
-  void* scratch = noalloc_scratch_address(dev);
-  if (scratch == nullptr) return ATTN_ECUDA;
-  const int BH = B * H;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
-    return ATTN_ECUDA;
-  uint64_t timeout;
-  int drop;
-  debug_settings(&timeout, &drop);
-  const float sl2 = scale * 1.4426950408889634f;
-  const size_t rows = static_cast<size_t>(BH) * Nq;
-  float* ws_o = static_cast<float*>(scratch);
-  float* ws_l = ws_o + static_cast<size_t>(num_splits) * rows * D;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st,
-                                   timeout, drop);
-  if (r != ATTN_OK) return r;
-  return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
-                 : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
+  if ((rc = check_keys_per_pass(Nq, Nk, causal, num_splits)) != ATTN_OK) return rc;
+  RunCtl run;
+  if ((rc = enter(&run, true)) != ATTN_OK) return rc;
+  return enqueue_splitkv(q, k, v, o, lse, B * H, Nq, Nk, D, scale, causal, num_splits, run.noalloc,
+                         static_cast<cudaStream_t>(stream), run);
 }
 
 int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
@@ -1298,33 +1422,25 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
   if ((lse_host == nullptr) != (lse_dev == nullptr)) return ATTN_EINVAL;
   if (num_chunks < 0 || num_chunks > kMaxHostChunks) return ATTN_EINVAL;
   bool empty = false;
-  const int rc = check_args(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Nq, Nk, D, scale, &empty);
+  int rc = check_args(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Nq, Nk, D, scale, &empty);
   if (rc != ATTN_OK || empty) return rc;
   const int BH = B * H;
   const size_t qb = static_cast<size_t>(BH) * Nq * D * 2, kb = static_cast<size_t>(BH) * Nk * D * 2;
   if (ranges_overlap(q_dev, qb, k_dev, kb) || ranges_overlap(q_dev, qb, v_dev, kb) ||
       ranges_overlap(k_dev, kb, v_dev, kb))
     return ATTN_EUNSUPPORTED;  // the device copies of the inputs are written here
-  const int sms = device_sms();
-  if (sms <= 0) return -sms;
+  if ((rc = check_keys_per_pass(Nq, Nk, causal, 0)) != ATTN_OK) return rc;
+  RunCtl run;
+  if ((rc = enter(&run)) != ATTN_OK) return rc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
   const int chunks = std::max(1, std::min(num_chunks == 0 ? 32 : num_chunks, BH));
-  uint64_t timeout;
-  int drop;
-  debug_settings(&timeout, &drop);
-  const float sl2 = scale * 1.4426950408889634f;
   auto compute = [&](int, int h0, int nb, cudaStream_t sc) -> int {
     const size_t qo = static_cast<size_t>(h0) * Nq * D, ko = static_cast<size_t>(h0) * Nk * D;
-    const __half* qc = static_cast<const __half*>(q_dev) + qo;
-    const __half* kc = static_cast<const __half*>(k_dev) + ko;
-    const __half* vc = static_cast<const __half*>(v_dev) + ko;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, qc, nb, Nq, D) || !make_map(&mk, kc, nb, Nk, D) || !make_map(&mv, vc, nb, Nk, D))
-      return ATTN_ECUDA;
-    return dispatch_fwd<false>(D, causal, mq, mk, mv, static_cast<__half*>(o_dev) + qo,
-                               lse_dev ? lse_dev + static_cast<size_t>(h0) * Nq : nullptr, nullptr, nullptr, nb, Nq,
-                               Nk, sl2, 1, sc, timeout, drop);
+    return enqueue_fwd(static_cast<const __half*>(q_dev) + qo, static_cast<const __half*>(k_dev) + ko,
+                       static_cast<const __half*>(v_dev) + ko, static_cast<__half*>(o_dev) + qo,
+                       lse_dev ? lse_dev + static_cast<size_t>(h0) * Nq : nullptr, nb, Nq, Nk, D, scale, causal, sc,
+                       run);
   };
   return host_pipeline(dev, q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev, BH, Nq,
                        Nk, D, 2, chunks, static_cast<cudaStream_t>(stream), compute);
@@ -1339,17 +1455,14 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  int D, float scale, int causal, float q_descale, float k_descale, float v_descale, void* workspace,
                  size_t workspace_bytes, void* stream) {
   bool empty = false;
-  const int rc = check_args_fp8(q, k, v, o, lse, B, H, Nq, Nk, D, scale, q_descale, k_descale, v_descale, workspace,
-                                workspace_bytes, &empty);
+  int rc = check_args_fp8(q, k, v, o, lse, B, H, Nq, Nk, D, scale, q_descale, k_descale, v_descale, workspace,
+                          workspace_bytes, &empty);
   if (rc != ATTN_OK || empty) return rc;
-  const int sms = device_sms();
-  if (sms <= 0) return -sms;
-  uint64_t timeout;
-  int drop;
-  debug_settings(&timeout, &drop);
+  RunCtl run;
+  if ((rc = enter(&run)) != ATTN_OK) return rc;
   const float sl2 = scale * q_descale * k_descale * 1.4426950408889634f;
   return enqueue_fp8(q, k, v, o, lse, workspace, 0, B * H, Nq, Nk, sl2, v_descale, causal,
-                     static_cast<cudaStream_t>(stream), timeout, drop);
+                     static_cast<cudaStream_t>(stream), run);
 }
 
 int attn_fwd_fp8_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
@@ -1360,26 +1473,23 @@ int attn_fwd_fp8_host(const void* q_host, const void* k_host, const void* v_host
   if ((lse_host == nullptr) != (lse_dev == nullptr)) return ATTN_EINVAL;
   if (num_chunks < 0 || num_chunks > kMaxHostChunks) return ATTN_EINVAL;
   bool empty = false;
-  const int rc = check_args_fp8(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Nq, Nk, D, scale, q_descale, k_descale,
-                                v_descale, workspace, workspace_bytes, &empty);
+  int rc = check_args_fp8(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Nq, Nk, D, scale, q_descale, k_descale,
+                          v_descale, workspace, workspace_bytes, &empty);
   if (rc != ATTN_OK || empty) return rc;
   const int BH = B * H;
   const size_t qb = static_cast<size_t>(BH) * Nq * D, kb = static_cast<size_t>(BH) * Nk * D;
   if (ranges_overlap(q_dev, qb, k_dev, kb) || ranges_overlap(q_dev, qb, v_dev, kb) ||
       ranges_overlap(k_dev, kb, v_dev, kb))
     return ATTN_EUNSUPPORTED;  // the device copies of the inputs are written here
-  const int sms = device_sms();
-  if (sms <= 0) return -sms;
+  RunCtl run;
+  if ((rc = enter(&run)) != ATTN_OK) return rc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
   const int chunks = std::max(1, std::min(num_chunks == 0 ? 32 : num_chunks, BH));
-  uint64_t timeout;
-  int drop;
-  debug_settings(&timeout, &drop);
   const float sl2 = scale * q_descale * k_descale * 1.4426950408889634f;
   auto compute = [&](int, int h0, int nb, cudaStream_t sc) -> int {
     return enqueue_fp8(q_dev, k_dev, v_dev, o_dev, lse_dev, workspace, h0, nb, Nq, Nk, sl2, v_descale, causal, sc,
-                       timeout, drop);
+                       run);
   };
   return host_pipeline(dev, q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev, BH, Nq,
                        Nk, D, 1, chunks, static_cast<cudaStream_t>(stream), compute);
@@ -1393,6 +1503,27 @@ int attn_debug_pack_e4m3(const float* in, unsigned int* out, int n_quads, void* 
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
+int attn_debug_exp2_poly(const float* in, float* out, int n, void* stream) {
+  if (n < 0) return ATTN_EINVAL;
+  if (n == 0) return ATTN_OK;
+  if (!in || !out) return ATTN_EINVAL;
+  const int pairs = (n + 1) / 2;
+  attn_debug_exp2_poly_kernel<<<(pairs + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(in, out, n);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
+}
+
+int attn_debug_fwd_poly_exp(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                            int Nk, int D, float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  if ((rc = check_keys_per_pass(Nq, Nk, causal, 0)) != ATTN_OK) return rc;
+  RunCtl run;
+  if ((rc = enter(&run)) != ATTN_OK) return rc;
+  return enqueue_fwd<kDebugEmu, kDebugEmu>(q, k, v, o, lse, B * H, Nq, Nk, D, scale, causal,
+                                           static_cast<cudaStream_t>(stream), run);
+}
+
 const char* attn_strerror(int code) {
   switch (code) {
     case ATTN_OK: return "ok";
@@ -1401,6 +1532,7 @@ const char* attn_strerror(int code) {
     case ATTN_ECUDA: return "CUDA error";
     case ATTN_ETIMEOUT: return "a kernel wait timed out";
     case ATTN_ESCRATCH: return "the problem needs more scratch than the library's built-in buffer holds";
+    case ATTN_ETOOLONG: return "more keys per row in one pass than the accuracy limit allows: use attn_fwd_splitkv";
     default: return "unknown error code";
   }
 }
@@ -1411,6 +1543,13 @@ int attn_get_status(void* stream) {
   const int zero = 0;
   if (cudaMemcpyFromSymbol(&h, g_attn_status, sizeof(int)) != cudaSuccess) return ATTN_ECUDA;
   if (h != 0 && cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ECUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  ContextState* st = nullptr;
+  if (context_state(&st) == ATTN_OK && st->status_host != nullptr) {
+    volatile int* mirror = st->status_host;
+    if (h == 0) h = *mirror;
+    *mirror = 0;
+  }
   return h;
 }
 

@@ -77,13 +77,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Shared state of the bounded waits of one CTA.  Every wait gives up after
 // `timeout_ns` of global time, raises the CTA's abort flag and records
-// `code` in the device status word; a wait that sees the abort flag raised
-// by another role gives up at once.  No wait in the kernel is unbounded.
+// `code` in the device status word and in its host copy (page-locked host
+// memory mapped into the device, or null); a wait that sees the abort flag
+// raised by another role gives up at once.  No wait in the kernel is
+// unbounded.
 struct WaitCtl {
   volatile int* abort_flag;  // shared memory
   int* status;               // global memory, first error wins
+  volatile int* status_host; // host copy, read by the host before each call
   uint64_t timeout_ns;
 };
+
+__device__ __forceinline__ void record_error(const WaitCtl& w, int code) {
+  atomicCAS(w.status, 0, code);
+  if (w.status_host != nullptr) {
+    *w.status_host = code;
+    __threadfence_system();
+  }
+}
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w,
                                           int code, bool honor_abort = true) {
@@ -94,7 +105,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (honor_abort && *w.abort_flag) return false;
     if (globaltimer_ns() - t0 > w.timeout_ns) {
       *w.abort_flag = 1;
-      atomicCAS(w.status, 0, code);
+      record_error(w, code);
       return false;
     }
   }

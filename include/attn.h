@@ -25,7 +25,8 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous on that stream; they perform no host synchronisation
  *     and no allocation, so they can be captured in a CUDA graph (make one
- *     ordinary call on the device first: it sets the kernels' attributes).
+ *     ordinary call on the device first: it sets the kernels' attributes and
+ *     creates the host copy of the device's status word, see attn_fwd).
  *   - Return values are ATTN_* codes below.  Argument errors are detected on
  *     the host before anything is enqueued.
  */
@@ -38,7 +39,7 @@
 extern "C" {
 #endif
 
-#define ATTN_VERSION 3
+#define ATTN_VERSION 4
 
 enum {
   ATTN_OK = 0,
@@ -46,9 +47,21 @@ enum {
   ATTN_EUNSUPPORTED = 2,  /* D not in {64,128}, misaligned pointer, overlapping output,
                              B*H > 65535, or a device other than sm_103 */
   ATTN_ECUDA = 3,         /* tensor-map encoding or kernel launch failed */
-  ATTN_ETIMEOUT = 4,      /* reported by attn_get_status: a kernel wait ran out */
-  ATTN_ESCRATCH = 5       /* attn_fwd_splitkv_noalloc: problem larger than the built-in scratch */
+  ATTN_ETIMEOUT = 4,      /* a kernel wait ran out: reported by attn_get_status, and by every
+                             call made while that report is pending */
+  ATTN_ESCRATCH = 5,      /* attn_fwd_splitkv_noalloc: problem larger than the built-in scratch */
+  ATTN_ETOOLONG = 6       /* more keys per row in one pass than ATTN_MAX_KEYS_PER_PASS: use
+                             attn_fwd_splitkv with more shares */
 };
+
+/* The most keys one row may accumulate in a single pass of the fp16 forward
+ * (2^19).  O is summed in fp32 by the tensor core over every key tile of the
+ * pass, and that sum drifts with the number of tiles: measured against an
+ * fp64 reference on N(0,1) data, the relative RMS error of O is 2.8e-4 at
+ * 2^16 keys, 5.8e-4 at 2^19 and 1.1e-3 at 2^20, past the 1e-3 this library
+ * is held to.  Longer rows go through attn_fwd_splitkv, whose shares are
+ * summed separately and merged in fp32 (2.1e-4 at 2^20 with 16 shares). */
+#define ATTN_MAX_KEYS_PER_PASS 524288
 
 /* Size of the device buffer compiled into the library for
  * attn_fwd_splitkv_noalloc (64 MiB on every device that loads the library). */
@@ -66,18 +79,20 @@ enum {
  *   scale  softmax scale, finite and >= 0 (the pages use 1/sqrt(D)).
  *   causal 0: every key is admissible; nonzero: key j masked when j > i.
  *
- * Accuracy: O is accumulated in fp32 by the tensor core over every key tile
- * of a row.  Measured against an fp64 reference on N(0,1) data, the relative
- * RMS error of O is 2.8e-4 at 2^16 keys, 5.8e-4 at 2^19 and 1.1e-3 at 2^20:
- * for key ranges beyond ~2^19 use attn_fwd_splitkv, whose shares accumulate
- * separately and are merged in fp32 (2.1e-4 at 2^20 with 16 shares).
+ * Key range: the keys one row accumulates -- Nk, or min(Nk, Nq) when causal
+ * -- must not exceed ATTN_MAX_KEYS_PER_PASS (2^19), else ATTN_ETOOLONG is
+ * returned and nothing is enqueued; attn_fwd_splitkv takes longer rows.
  *
- * Errors: ATTN_EINVAL / ATTN_EUNSUPPORTED for bad arguments (nothing is
- * enqueued), ATTN_ECUDA if encoding the TMA descriptors or the launch fails.
- * A kernel whose internal wait runs out stops early, leaves o / lse
- * undefined and records ATTN_ETIMEOUT for attn_get_status().  While that
- * status word is set, later launches on the device do no work (their
- * outputs are undefined) until attn_get_status() reads and clears it.
+ * Errors: ATTN_EINVAL / ATTN_EUNSUPPORTED / ATTN_ETOOLONG for bad arguments
+ * (nothing is enqueued), ATTN_ECUDA if encoding the TMA descriptors or the
+ * launch fails.  A kernel whose internal wait runs out stops early, leaves
+ * o / lse undefined and records ATTN_ETIMEOUT in the device's status word,
+ * of which the library keeps a copy in page-locked host memory.  From the
+ * moment that copy shows the error until attn_get_status() reads and clears
+ * it, every forward entry point returns ATTN_ETIMEOUT at once, without
+ * enqueueing anything and without synchronising; launches that were already
+ * enqueued when the error was recorded do no work (their outputs are
+ * undefined).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
              int Nk, int D, float scale, int causal, void* stream);
@@ -133,7 +148,12 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
  *
  *   q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, stream: as attn_fwd.
  *   num_splits  1 .. 256 shares (attn_splitkv_suggest gives one); shares
- *               that hold no admissible key are allowed.
+ *               that hold no admissible key are allowed.  A share holds
+ *               ceil(T / num_splits) key tiles of 128 at most, T being the
+ *               key tiles of the longest query-tile pair (ceil(Nk / 128); when
+ *               causal, ceil(min(Nk, Nq rounded up to 256) / 128)); that times
+ *               128 must not exceed ATTN_MAX_KEYS_PER_PASS, else
+ *               ATTN_ETOOLONG.
  *   workspace   device memory owned by the caller, 16-byte aligned, at least
  *               attn_splitkv_workspace_bytes(B, H, Nq, D, num_splits) bytes,
  *               not overlapping any tensor argument.  Its contents on entry
@@ -142,7 +162,8 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
  *
  * Enqueues two kernels on `stream`.  Errors as attn_fwd, plus ATTN_EINVAL for
  * num_splits outside 1..256 or a missing / too small workspace and
- * ATTN_EUNSUPPORTED for a misaligned or overlapping workspace.
+ * ATTN_EUNSUPPORTED for a misaligned or overlapping workspace.  The merge
+ * kernel, too, does nothing while the device's status word holds an error.
  */
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int Nq, int Nk, int D, float scale, int causal, int num_splits, void* workspace,
@@ -153,8 +174,9 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
 size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
 
 /* A share count for the current device: enough CTAs to fill its SMs once,
- * with at least four 128-key tiles per share.  Returns >= 1, or 0 for bad
- * arguments or when the current device is not supported. */
+ * with at least four 128-key tiles per share, and enough shares to keep each
+ * within ATTN_MAX_KEYS_PER_PASS.  Returns >= 1, or 0 for bad arguments or
+ * when the current device is not supported. */
 int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal);
 
 /*
@@ -173,9 +195,11 @@ int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal);
  *     num_splits * B * H * Nq * (D + 1) * 4 <= ATTN_NOALLOC_SCRATCH_BYTES,
  *   else ATTN_ESCRATCH is returned and nothing is enqueued.
  *   The buffer is held by every device that loads the library, until the
- *   process exits.  The first call on a device looks up the buffer's device
- *   address (a runtime query that allocates nothing); make that first call
- *   before any stream capture.
+ *   process exits.  Every call looks up the buffer's device address with
+ *   cudaGetSymbolAddress (a runtime query that allocates nothing), so the
+ *   address stays right after a context reset.  The first call on a device
+ *   loads the library's kernels there; make that first call before any
+ *   stream capture.
  *   Every call uses the same buffer, which keeps the last call's contents;
  *   nothing in it needs to start at zero (each part is written before it
  *   is read).  Calls whose kernels overlap on the GPU race on the buffer:
@@ -248,13 +272,35 @@ size_t attn_fp8_workspace_bytes(int B, int H, int Nk, int D);
  */
 int attn_debug_pack_e4m3(const float* in, unsigned int* out, int n_quads, void* stream);
 
+/*
+ * Testing hook: the FMA-pipe 2^x of the forward ("the FMA-emulated exp" of
+ * FlashAttention-4 in "Relationship to FA-3 and FA-4": Cody-Waite reduction
+ * to [-1/2, 1/2], a degree-4 minimax polynomial, the exponent added to the
+ * float's exponent field), on its own.  in, out: n fp32 values (device);
+ * out[i] = 2^in[i] with relative error below 4e-6 for -126 <= in[i] <= 127;
+ * inputs below -126, and NaN, give 2^-126.  Asynchronous on `stream`.
+ * n = 0 does nothing (the pointers may then be NULL); ATTN_EINVAL for null
+ * pointers with n > 0, or n < 0.
+ */
+int attn_debug_exp2_poly(const float* in, float* out, int n, void* stream);
+
+/*
+ * Testing hook: attn_fwd with one pair of exponentials in four taken by the
+ * FMA-pipe polynomial above instead of the exponential unit (the forward
+ * itself uses the exponential unit alone: on GB300 the split measured
+ * slower).  Arguments, results and errors as attn_fwd.
+ */
+int attn_debug_fwd_poly_exp(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int Nq, int Nk, int D, float scale, int causal, void* stream);
+
 /* Human-readable text for an ATTN_* code.  Never NULL. */
 const char* attn_strerror(int code);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
- * word: ATTN_OK, or the first error a kernel recorded since the last call
- * (ATTN_ETIMEOUT).  Returns ATTN_ECUDA if the synchronisation itself fails.
+ * word and its host copy: ATTN_OK, or the first error a kernel recorded
+ * since the last call (ATTN_ETIMEOUT).  Returns ATTN_ECUDA if the
+ * synchronisation itself fails.
  */
 int attn_get_status(void* stream);
 

@@ -32,8 +32,13 @@ def run_gpu(q, k, v, scale, causal):
     return o.cpu().numpy(), lse.cpu().numpy()
 
 
-def compare(o_gpu, lse_gpu, O_ref, L_ref, label=""):
-    """Element-wise comparison; returns the three error figures."""
+def compare(o_gpu, lse_gpu, O_ref, L_ref, label="", sigma_v=1.0):
+    """Element-wise comparison; returns the three error figures.
+
+    The O max-abs bound is stated for V of unit scale (every workload draws
+    V from N(0, 1)); O is linear in V, so for V drawn with standard deviation
+    sigma_v the bound is TOL_O_MAXABS * sigma_v.  The relative RMS bound is
+    scale-free and the LSE does not depend on V."""
     o = o_gpu.astype(np.float64).reshape(O_ref.shape)
     l = lse_gpu.astype(np.float64).reshape(L_ref.shape)
     assert np.all(np.isfinite(o)), f"{label}: non-finite O"
@@ -43,7 +48,7 @@ def compare(o_gpu, lse_gpu, O_ref, L_ref, label=""):
     nrm = float(np.linalg.norm(O_ref))
     rel_rms = float(np.linalg.norm(diff) / nrm) if nrm > 0 else float(np.linalg.norm(diff))
     lse_err = float(np.abs(l - L_ref).max())
-    assert max_abs <= TOL_O_MAXABS, f"{label}: O max-abs {max_abs:.3e}"
+    assert max_abs <= TOL_O_MAXABS * sigma_v, f"{label}: O max-abs {max_abs:.3e}"
     assert rel_rms <= TOL_O_RELRMS, f"{label}: O rel-RMS {rel_rms:.3e}"
     assert lse_err <= TOL_LSE_MAXABS, f"{label}: LSE max-abs {lse_err:.3e}"
     return max_abs, rel_rms, lse_err
@@ -54,4 +59,4 @@ def full_parity(B, H, Nq, Nk, D, causal, seed, sigma_qk=1.0, sigma_v=1.0, scale=
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     o, lse = run_gpu(q, k, v, scale, causal)
     O, L = oracle.attn_full(q, k, v, scale, causal)
-    return compare(o, lse, O, L, f"[{B},{H},{Nq},{Nk},{D}] causal={causal}")
+    return compare(o, lse, O, L, f"[{B},{H},{Nq},{Nk},{D}] causal={causal}", sigma_v=sigma_v)

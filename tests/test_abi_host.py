@@ -35,10 +35,18 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert attn.version() == 3
+    assert attn.version() == 4
     for code in (attn.ATTN_OK, attn.ATTN_EINVAL, attn.ATTN_EUNSUPPORTED, attn.ATTN_ECUDA,
-                 attn.ATTN_ETIMEOUT, 99):
+                 attn.ATTN_ETIMEOUT, attn.ATTN_ESCRATCH, attn.ATTN_ETOOLONG, 99):
         assert isinstance(attn.strerror(code), str) and attn.strerror(code)
+    assert "splitkv" in attn.strerror(attn.ATTN_ETOOLONG)
+    assert attn.strerror(attn.ATTN_ETOOLONG) != attn.strerror(99)
+
+
+def test_header_constants_match_binding(lib):
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    assert int(re.search(r"#define ATTN_MAX_KEYS_PER_PASS (\d+)", text).group(1)) == attn.MAX_KEYS_PER_PASS
+    assert int(re.search(r"ATTN_ETOOLONG = (\d+)", text).group(1)) == attn.ATTN_ETOOLONG
 
 
 A = 1 << 20  # a 16-byte aligned fake address: validation never dereferences it
@@ -61,6 +69,28 @@ A = 1 << 20  # a 16-byte aligned fake address: validation never dereferences it
 ])
 def test_argument_validation_without_device(lib, args, code):
     assert attn.attn_fwd(*args, None) == code
+
+
+FAR = 1 << 40  # an output address far from the fake inputs, so no overlap is reported
+LONG = (1 << 19) + 1  # one key more than a single pass may accumulate per row
+
+
+@pytest.mark.parametrize("Nq,Nk,causal,code", [
+    (8, LONG, 0, attn.ATTN_ETOOLONG),      # non-causal: every row accumulates Nk keys
+    (LONG, LONG, 1, attn.ATTN_ETOOLONG),   # causal: the last row accumulates min(Nk, Nq) keys
+])
+def test_key_range_beyond_one_pass_is_rejected_without_device(lib, Nq, Nk, causal, code):
+    assert attn.attn_fwd(A, A, A, FAR, None, 1, 1, Nq, Nk, 64, 0.1, causal, None) == code
+    assert attn.attn_debug_fwd_poly_exp(A, A, A, FAR, None, 1, 1, Nq, Nk, 64, 0.1, causal, None) == code
+
+
+def test_split_kv_share_beyond_one_pass_is_rejected_without_device(lib):
+    W2 = 1 << 44  # workspace far from everything
+    nk = 2 * (1 << 19) + 128  # 8193 key tiles: two shares hold 4097 tiles, one more than a pass
+    f = attn.attn_fwd_splitkv
+    assert f(A, A, A, FAR, None, 1, 1, 8, nk, 64, 0.1, 0, 2, W2, 1 << 30, None) == attn.ATTN_ETOOLONG
+    g = attn.attn_fwd_splitkv_noalloc
+    assert g(A, A, A, FAR, None, 1, 1, 8, nk, 64, 0.1, 0, 2, None) == attn.ATTN_ETOOLONG
 
 
 def test_debug_hook_validation(lib):

@@ -1,7 +1,9 @@
 """Failure detection on the GPU without a fault: one TMA load is never
 issued (attn_debug_set's drop_kv_tile), so the wait for it runs out after a
 short limit; the kernel must stop cleanly, report ATTN_ETIMEOUT through
-attn_get_status, and leave the context usable for the next correct call."""
+attn_get_status -- and, until that report is read, through every call, at
+once and without a device synchronisation -- and leave the context usable
+for the next correct call."""
 import math
 
 import numpy as np
@@ -27,10 +29,16 @@ def test_dropped_load_times_out_and_context_survives(D):
         assert attn.debug_set(50_000_000, 1) == attn.ATTN_OK  # 50 ms limit, key tile 1 never loaded
         attn.fwd(q, k, v, causal=False)
         torch.cuda.synchronize()
-        assert attn.get_status() == attn.ATTN_ETIMEOUT
-        assert attn.get_status() == attn.ATTN_OK  # read-and-clear
     finally:
         attn.debug_set(2_000_000_000, -1)
+    # The error is pending: every entry point refuses to enqueue, without a sync.
+    for call in (lambda: attn.fwd(q, k, v, causal=False),
+                 lambda: attn.fwd_splitkv(q, k, v, num_splits=2)):
+        with pytest.raises(attn.AttnError) as e:
+            call()
+        assert e.value.code == attn.ATTN_ETIMEOUT
+    assert attn.get_status() == attn.ATTN_ETIMEOUT
+    assert attn.get_status() == attn.ATTN_OK  # read-and-clear
     o, lse = attn.fwd(q, k, v, causal=False)
     torch.cuda.synchronize()
     assert attn.get_status() == attn.ATTN_OK
