@@ -1369,11 +1369,29 @@ int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal) {
   }
   const int64_t ctas = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
   const int64_t tiles = pair_key_tiles(Nq, Nk, causal);
-  int64_t s = (sms + ctas - 1) / ctas;               // fill the SMs once
-  s = std::min<int64_t>(s, std::max<int64_t>(1, tiles / 4));  // at least 4 key tiles per share
-  // no share longer than one pass may accumulate
-  s = std::max<int64_t>(s, (tiles * kBlockN + ATTN_MAX_KEYS_PER_PASS - 1) / ATTN_MAX_KEYS_PER_PASS);
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits)));
+  // No share may hold more keys than one pass may accumulate.
+  const int64_t s_min = std::max<int64_t>(1, (tiles * kBlockN + ATTN_MAX_KEYS_PER_PASS - 1) / ATTN_MAX_KEYS_PER_PASS);
+  // At least four key tiles per share, at most 256 shares.
+  const int64_t s_max = std::max<int64_t>(s_min, std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, tiles / 4)));
+  // Cost model in key-tile steps of one CTA (~1.1-1.4 us on GB300), fitted
+  // to split-KV timings of decode and prefill shapes: waves of CTAs times
+  // (the tiles of a share + ~5 steps of start-up and epilogue per CTA); a
+  // split adds the merge launch (~8 steps) and the fp32 parts it writes and
+  // reads back ((D+1)*4 bytes per row and share, both ways, at ~8 MB per
+  // step).  One share means the single pass (no parts, no merge).
+  const double rows = static_cast<double>(B) * H * Nq;
+  int64_t best = s_min;
+  double best_cost = 1e300;
+  for (int64_t s = s_min; s <= s_max; ++s) {
+    const double waves = static_cast<double>((ctas * s + sms - 1) / sms);
+    double cost = waves * (static_cast<double>((tiles + s - 1) / s) + 5.0);
+    if (s > 1) cost += 8.0 + rows * (D + 1) * 8.0 * static_cast<double>(s) / 8.0e6;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return static_cast<int>(std::min<int64_t>(best, kMaxSplits));
 }
 
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,

@@ -173,9 +173,13 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
  * 0 for negative sizes, D not in {64,128} or num_splits outside 1..256. */
 size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
 
-/* A share count for the current device: enough CTAs to fill its SMs once,
- * with at least four 128-key tiles per share, and enough shares to keep each
- * within ATTN_MAX_KEYS_PER_PASS.  Returns >= 1, or 0 for bad arguments or
+/* A share count for the current device, from a cost model of the kernels
+ * measured on GB300: waves of CTAs times the key tiles of a share plus a
+ * fixed cost per CTA, and for a split the merge and the fp32 parts written
+ * and read back.  1 means the single pass (attn_fwd) is expected to be
+ * faster: a grid that already fills the SMs gains nothing from shares.
+ * Shares hold at least four 128-key tiles and at most
+ * ATTN_MAX_KEYS_PER_PASS keys.  Returns >= 1, or 0 for bad arguments or
  * when the current device is not supported. */
 int attn_splitkv_suggest(int B, int H, int Nq, int Nk, int D, int causal);
 

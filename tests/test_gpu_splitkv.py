@@ -72,3 +72,18 @@ def test_splitkv_suggest_fills_the_gpu():
     s = attn.splitkv_suggest(1, 8, 1, 32768, 128, False)
     assert 2 <= s <= 256
     assert attn.splitkv_suggest(4, 32, 16384, 16384, 128, False) == 1
+
+
+def test_share_suggestion_follows_the_measured_cost():
+    """The suggested share count splits decode-like shapes (few CTAs, many
+    keys) and leaves shapes whose grid already fills the SMs to the single
+    pass (the split-KV path then only adds the parts and the merge)."""
+    torch_cuda()
+    import attention_forward_12_gb300 as attn
+    assert attn.splitkv_suggest(1, 8, 4096, 4096, 64, False) == 1      # 128 CTAs
+    assert attn.splitkv_suggest(1, 16, 8192, 8192, 128, False) == 1    # 512 CTAs
+    assert attn.splitkv_suggest(1, 8, 128, 32768, 128, False) >= 8     # 8 CTAs, 256 key tiles
+    assert attn.splitkv_suggest(4, 8, 1, 65536, 128, False) >= 4       # 32 CTAs, 512 key tiles
+    # 2^20 keys: never a share longer than one pass may accumulate
+    s = attn.splitkv_suggest(1, 1, 3, 1 << 20, 64, False)
+    assert s >= 2 and (8192 + s - 1) // s * 128 <= attn.MAX_KEYS_PER_PASS
