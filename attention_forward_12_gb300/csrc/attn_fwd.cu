@@ -103,9 +103,11 @@ struct Layout {
   static constexpr int kChunkElems = 128 / kElem;
   static constexpr uint32_t kTileBytes = kBlockM * HD * kElem;  // one Q, K or V tile
   // q_full, k/v full/empty[NS], s_full/p_half/p_full[3] (one per TMEM score
-  // slot), o_done[4], drain
-  static constexpr int kBars = 1 + 4 * NS + 3 * 3 + 4 + 1;
-  static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
+  // slot), o_done[4], drain, xchg; then the TMEM address, the abort flag and
+  // the last loads per stage, and the (m, d) exchange of a single-tile CTA
+  static constexpr int kBars = 1 + 4 * NS + 3 * 3 + 4 + 1 + 1;
+  static constexpr size_t kXchgBytes = 2 * 2 * kBlockM * sizeof(float);
+  static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8 + kXchgBytes;
 };
 
 // Key tiles query tile w of the CTA visits (0 if the tile lies past Nq).
@@ -204,13 +206,13 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[4][32], float2 sl2
 // recorded since the last attn_get_status().
 __device__ int g_attn_status;
 
-template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8, int SLOTS>
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8, int SLOTS, bool SINGLE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
                 float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_l, int Nq, int Nk,
                 float sl2, float o_scale, int* status_host, uint64_t timeout_ns,
-                int drop_tile) {
+                int drop_tile, int n_main) {
   static_assert(!FP8 || HD == 128, "the E4M3 kernel is built for D = 128 only");
   static_assert(SPLIT_P == 0 || SPLIT_P == 2, "P released whole (0) or in two halves (2)");
   using L = Layout<HD, NS, FP8>;
@@ -233,28 +235,56 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   uint64_t* o_done = p_full + 3;    // [4] completed O_w += P_w V_j: SLOTS = 2: [w], one phase per
                                     // product; SLOTS = 3: [2w + (j & 1)], one phase per two
   uint64_t* drain = o_done + 4;     // abort path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xchg = drain + 1;       // single-tile CTA: both warpgroups' (m, d) written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* last_k = abort_flag + 1;     // [NS] last tile loaded per stage (abort drain)
   int* last_v = last_k + NS;
+  float* x_m = reinterpret_cast<float*>(last_v + NS);  // [2][128] single-tile CTA: m per warpgroup and row
+  float* x_d = x_m + 2 * kBlockM;                      // [2][128] d per warpgroup and row
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  // Work of this CTA.  Usually two query tiles of one (batch, head) -- a
+  // pair -- each warpgroup taking one of them against every key tile (of the
+  // share, with split-KV).  SINGLE (the non-causal fp16 D = 128 forward):
+  // one query tile, both warpgroups sharing its key range -- warpgroup w
+  // takes key tiles w, w + 2, ... -- and merging their two partial results
+  // at the end.  The host runs the pairs of a last partial wave that would
+  // occupy at most half the SMs this way, as a second launch of twice as
+  // many CTAs doing half the work each: the pairs' launch skips them
+  // (n_main: the pairs it keeps, in (head, pair) order), and the single-
+  // tile launch's CTA b takes query tile b % 2 of pair n_main + b / 2.
+  constexpr bool single = SINGLE;
+  static_assert(!SINGLE || (SLOTS == 2 && SPLIT_P == 2 && !FP8 && !SPLITKV && !CAUSAL), "single-tile CTAs");
+  int bh, pair, half = 0;
+  if constexpr (SINGLE) {
+    const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
+    const int b = static_cast<int>(blockIdx.x);
+    const int item = n_main + (b >> 1);
+    half = b & 1;
+    pair = item % n_pairs;
+    bh = item / n_pairs;
+  } else {
+    bh = static_cast<int>(blockIdx.y);
+    pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+    if (static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) >= n_main) return;  // left to the single-tile launch
+  }
   const int r0 = pair * kRowsPerCta;
   // Key tiles of this CTA: all of the pair's (grid z = 1), or with split-KV
   // the contiguous share [t0, t1) of split blockIdx.z.  nkv0 / nkv1 count the
-  // tiles each query tile visits in that share (0 if the tile lies past Nq
-  // or, when causal, if its diagonal comes before the share).
-  const int nkv0_all = tile_kv_count<CAUSAL>(r0, Nq, Nk);
-  const int nkv1_all = tile_kv_count<CAUSAL>(r0 + kBlockM, Nq, Nk);
+  // tiles each warpgroup visits in that share (0 if its query tile lies past
+  // Nq or, when causal, if its diagonal comes before the share); nkv counts
+  // the K/V tiles the producer loads.
+  const int nkv0_all = single ? 0 : tile_kv_count<CAUSAL>(r0, Nq, Nk);
+  const int nkv1_all = single ? 0 : tile_kv_count<CAUSAL>(r0 + kBlockM, Nq, Nk);
   const int nkv_all = max(nkv0_all, nkv1_all);
   const int t0 = SPLITKV ? static_cast<int>(static_cast<int64_t>(nkv_all) * blockIdx.z / gridDim.z) : 0;
   const int t1 = SPLITKV ? static_cast<int>(static_cast<int64_t>(nkv_all) * (blockIdx.z + 1) / gridDim.z) : nkv_all;
-  const int nkv0 = SPLITKV ? max(0, min(t1, nkv0_all) - t0) : nkv0_all;
-  const int nkv1 = SPLITKV ? max(0, min(t1, nkv1_all) - t0) : nkv1_all;
-  const int nkv = max(nkv0, nkv1);
+  const int nkv_single = single ? tile_kv_count<CAUSAL>(r0 + half * kBlockM, Nq, Nk) : 0;
+  const int nkv0 = single ? (nkv_single + 1) / 2 : SPLITKV ? max(0, min(t1, nkv0_all) - t0) : nkv0_all;
+  const int nkv1 = single ? nkv_single / 2 : SPLITKV ? max(0, min(t1, nkv1_all) - t0) : nkv1_all;
+  const int nkv = single ? nkv_single : max(nkv0, nkv1);
   const size_t rows_total = static_cast<size_t>(gridDim.y) * Nq;  // split-KV part stride
 
   // A CTA of a launch that already recorded an error does no work: after a
@@ -263,6 +293,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) *abort_flag = *static_cast<volatile int*>(&g_attn_status);
   __syncthreads();
   if (*abort_flag) return;
+  if (single && nkv == 0) return;  // a single query tile past Nq: nothing to do
   if constexpr (SPLITKV) {
     if (nkv == 0) {
       // No admissible key in this share for either tile: an empty part
@@ -296,6 +327,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     for (int b = 0; b < 4; ++b) mbar_init(&o_done[b], 1);
     mbar_init(drain, 1);
+    mbar_init(xchg, 2 * kBlockM);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -331,11 +363,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(q_full, (nkv0 > 0 ? TB : 0) + (nkv1 > 0 ? TB : 0));
+      // A single-tile CTA loads its one query tile into the first Q buffer,
+      // which both warpgroups' Q K^T read.
+      const int q0_row = single ? r0 + half * kBlockM : r0;
+      const bool load_q1 = !single && nkv1 > 0;
+      mbar_arrive_expect_tx(q_full, (nkv0 > 0 ? TB : 0) + (load_q1 ? TB : 0));
       if (nkv0 > 0)
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * L::kChunkElems, r0, bh);
-      if (nkv1 > 0)
+          tma_load_3d(sQ + c * kChunkBytes, &tmQ, q_full, c * L::kChunkElems, q0_row, bh);
+      if (load_q1)
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sQ + TB + c * kChunkBytes, &tmQ, q_full, c * L::kChunkElems, r0 + kBlockM, bh);
       bool ok = true;
@@ -395,7 +431,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // reduction over D runs in steps of 16 (32 bytes inside a swizzle row).
     auto issue_s = [&](int w, int s, int slot) {
       const uint32_t dS = tmem + slot * 128;
-      const uint64_t a = dQ + ((w * TB) >> 4);
+      const uint64_t a = dQ + (((single ? 0 : w) * TB) >> 4);  // a single-tile CTA has one Q tile
       const uint64_t b = dK + ((s * TB) >> 4);
 #pragma unroll
       for (int kk = 0; kk < kQkSteps; ++kk) {
@@ -441,7 +477,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       return true;
     };
-    if constexpr (SLOTS == 2) {
+    if constexpr (SINGLE) {
+      // Single query tile: warpgroup w takes key tiles w, w + 2, ...; key
+      // tile t lives in stage t % NS.  Its local tile index jj = t / 2
+      // selects the parity of its slot, P and o_done phases (one per tile
+      // of that warpgroup).  K stages are released after their Q K^T, V
+      // stages after their P V, so the producer's K loads stay a tile pair
+      // ahead.
+      auto st = [](int t) { return t % NS; };
+      auto ph = [](int t) { return static_cast<uint32_t>((t / NS) & 1); };
+      bool ok = wait_all(q_full, 0);
+      for (int t = 0; t < 2 && t < nkv && ok; ++t) {
+        if (!(ok = wait_all(&k_full[st(t)], ph(t)))) break;
+        issue_s(t, st(t), t);
+        umma_commit_warp(&k_empty[st(t)]);
+      }
+      for (int t = 0; t < nkv && ok; ++t) {
+        const int w = t & 1, jj = t >> 1;
+        if (!(ok = wait_all(&v_full[st(t)], ph(t)))) break;
+        if (!(ok = issue_pv(w, jj, st(t), w, static_cast<uint32_t>(jj & 1)))) break;
+        umma_commit_warp(&v_empty[st(t)]);
+        if (t + 2 < nkv) {
+          if (!(ok = wait_all(&k_full[st(t + 2)], ph(t + 2)))) break;
+          issue_s(w, st(t + 2), w);
+          umma_commit_warp(&k_empty[st(t + 2)]);
+        }
+      }
+    } else if constexpr (SLOTS == 2) {
       bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
       if (ok) {
         if (nkv0 > 0) issue_s(0, 0, 0);
@@ -508,9 +570,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int wg = warp >> 2;             // query tile of this warpgroup
+    const int wg = warp >> 2;             // query tile of this warpgroup (a single-tile CTA: key tile parity)
     const int row = threadIdx.x & 127;    // tile row == TMEM lane
-    const int rw = r0 + wg * kBlockM;
+    const int rw = single ? r0 + half * kBlockM : r0 + wg * kBlockM;
     const int i = rw + row;
     const int my_nkv = wg ? nkv1 : nkv0;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -570,7 +632,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[slot], par, wc, ATTN_ETIMEOUT));
       if (!ok) break;
       tc_fence_after();
-      const int key0 = (t0 + j) * kBlockN;
+      const int key0 = (t0 + (single ? 2 * j + wg : j)) * kBlockN;
       const bool masked = (key0 + kBlockN > Nk) || (CAUSAL && key0 + kBlockN - 1 > rw);
       const int lim = row_lim - key0;  // columns [0, lim) of this tile are admissible
       // The reducing TMEM load hands back each row's maximum with its
@@ -661,7 +723,60 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else {
       if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[wg], (my_nkv - 1) & 1, wc, ATTN_ETIMEOUT));
     }
-    if (ok && my_nkv > 0 && !SPLITKV) {
+    if (single && ok) {
+      // ------------------------------------ single-tile CTA: merge, epilogue
+      // Each warpgroup holds the carrier of its half of the key tiles for
+      // the same 128 rows: (m_w, d_w) in registers, O_w in TMEM.  The carrier
+      // merge: m = max(m0, m1), a_w = 2^(m_w - m), O = (a0 O0 + a1 O1) /
+      // (a0 d0 + a1 d1).  The (m, d) pairs go through shared memory; then
+      // warpgroup w writes columns [64 w, 64 w + 64) of every row, reading
+      // them from both O accumulators (any warp may read the TMEM lanes of
+      // its sub-partition, whichever warpgroup accumulated them).
+      x_m[wg * kBlockM + row] = m_ref;
+      x_d[wg * kBlockM + row] = dsum;
+      mbar_arrive(xchg);
+      ok = __all_sync(0xffffffffu, mbar_wait(xchg, 0, wc, ATTN_ETIMEOUT));
+      if (ok) {
+        tc_fence_after();
+        const float m0 = x_m[row], m1 = x_m[kBlockM + row];
+        const float m = fmaxf(m0, m1);  // m0 is finite: warpgroup 0 always has a key tile
+        const float a0 = ex2_approx(m0 - m);
+        const float a1 = nkv1 > 0 ? ex2_approx(m1 - m) : 0.f;
+        const float d = a0 * x_d[row] + a1 * x_d[kBlockM + row];
+        const float inv = 1.f / d;
+        const float2 c0 = make_float2(a0 * inv, a0 * inv), c1 = make_float2(a1 * inv, a1 * inv);
+        const uint32_t tO0 = tmem + kOCol + lane_off, tO1 = tmem + kOCol + kOStride + lane_off;
+        __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
+#pragma unroll
+        for (int cc = 0; cc < HD / 64; ++cc) {
+          const int c = wg * (HD / 64) + cc;  // this warpgroup's 32-column chunks
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO0 + c * 32, o0);
+          if (nkv1 > 0) tmem_ld32(tO1 + c * 32, o1);
+          tmem_ld_wait(o0);
+          if (nkv1 > 0) {
+            tmem_ld_wait(o1);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o1[e] = 0u;
+          }
+          if (i < Nq) {
+            uint32_t h[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 v = __ffma2_rn(make_float2(__uint_as_float(o1[2 * e]), __uint_as_float(o1[2 * e + 1])), c1,
+                                          __fmul2_rn(make_float2(__uint_as_float(o0[2 * e]), __uint_as_float(o0[2 * e + 1])), c0));
+              h[e] = pack_half2(v.x, v.y);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+          }
+        }
+        if (wg == 0 && lse != nullptr && i < Nq)
+          lse[static_cast<size_t>(bh) * Nq + i] = (m + log2f(d)) * 0.69314718055994531f;
+      }
+    } else if (ok && my_nkv > 0 && !SPLITKV) {
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
       const float inv = o_scale / dsum;  // o_scale: the E4M3 kernel's V descale, else 1
@@ -1050,12 +1165,13 @@ int enter(RunCtl* rc, bool want_noalloc = false) {
 }
 
 // ------------------------------------------------------------ launches
-template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
-int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
-               float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
-               const RunCtl& rc, float o_scale = 1.0f) {
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2,
+          bool SINGLE = false>
+int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
+                  float* ws_o, float* ws_l, dim3 grid, int Nq, int Nk, float sl2, int n_main, cudaStream_t st,
+                  const RunCtl& rc, float o_scale) {
   using L = Layout<HD, NS, FP8>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS>;
+  auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, SINGLE>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
   // The shared-memory attribute is set on the first launch on each device
   // only: the host-buffer entry points launch once per chunk, and every
@@ -1070,9 +1186,8 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
       return ATTN_ECUDA;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, BH, splits);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop);
+                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
   if (cudaGetLastError() == cudaSuccess) return ATTN_OK;
   // A context reset (cudaDeviceReset) drops the attribute: set it again and
   // retry once (a launch that failed did not run).
@@ -1082,8 +1197,41 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     return ATTN_ECUDA;
   attr_set.fetch_or(bit, std::memory_order_release);
   kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop);
+                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
+}
+
+// One forward: the grid of (query-tile pair, head, share) CTAs.  For the
+// non-causal fp16 D = 128 single pass, the pairs of a last partial wave that
+// would occupy at most half the SMs go to a second launch of single-tile
+// CTAs (two per pair, half the work each), which runs as soon as the full
+// waves are done: that wave then takes half as long.
+template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
+int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
+               float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
+               const RunCtl& rc, float o_scale = 1.0f) {
+  const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
+  constexpr bool kTail = HD == 128 && SLOTS == 2 && SPLIT_P == 2 && !FP8 && !SPLITKV && !CAUSAL;
+  int64_t tail = 0;
+  if (kTail && rc.sms > 0) {
+    const int64_t last = pairs % rc.sms;
+    if (last > 0 && 2 * last <= rc.sms) tail = last;
+  }
+  if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
+  const int n_main = static_cast<int>(pairs - tail);
+  if (n_main > 0) {
+    const int r = launch_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, false>(
+        mq, mk, mv, o, lse, ws_o, ws_l, dim3(n_pairs, BH, splits), Nq, Nk, sl2, n_main, st, rc, o_scale);
+    if (r != ATTN_OK) return r;
+  }
+  if constexpr (kTail) {
+    if (tail > 0)
+      return launch_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, true>(
+          mq, mk, mv, o, lse, ws_o, ws_l, dim3(static_cast<unsigned>(2 * tail)), Nq, Nk, sl2, n_main, st, rc,
+          o_scale);
+  }
+  return ATTN_OK;
 }
 
 // The fp16 forward: D = 64 with three rotating score slots and P released
