@@ -18,7 +18,7 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 MAX_KEYS_PER_PASS = 1 << 19
 
 # Every symbol the C header declares; the CPU tests check they are exported.
-EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
+EXPORTS = ("attn_fwd", "attn_fwd_launch_count", "attn_fwd_host", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes", "attn_splitkv_suggest",
            "attn_fwd_splitkv_noalloc", "attn_fwd_fp8", "attn_fwd_fp8_host", "attn_fp8_workspace_bytes", "attn_debug_pack_e4m3",
            "attn_debug_exp2_poly", "attn_debug_fwd_poly_exp", "attn_strerror", "attn_get_status", "attn_debug_set",
            "attn_version")
@@ -47,6 +47,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd.restype = i32
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, vp]
+            lib.attn_fwd_launch_count.restype = i32
+            lib.attn_fwd_launch_count.argtypes = [i32] * 6
             lib.attn_fwd_host.restype = i32
             lib.attn_fwd_host.argtypes = [vp] * 10 + [i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp]
             lib.attn_fwd_splitkv.restype = i32
@@ -98,6 +100,11 @@ def attn_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int | None
     return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
                                    int(Nq), int(Nk), int(D), float(scale), int(bool(causal)),
                                    stream)
+
+
+def fwd_launch_count(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool) -> int:
+    """Kernels attn_fwd enqueues for these sizes on the current device (1 or 2)."""
+    return int(load_library().attn_fwd_launch_count(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal))))
 
 
 def attn_fwd_host(qh: int, kh: int, vh: int, oh: int, lh: int | None, qd: int, kd: int, vd: int, od: int,

@@ -1206,6 +1206,14 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 // would occupy at most half the SMs go to a second launch of single-tile
 // CTAs (two per pair, half the work each), which runs as soon as the full
 // waves are done: that wave then takes half as long.
+// Pairs of the last partial wave that go to single-tile CTAs: all of the
+// last wave's pairs when it would occupy at most half of the `sms` SMs.
+int64_t tail_pairs(int64_t pairs, int sms) {
+  if (sms <= 0) return 0;
+  const int64_t last = pairs % sms;
+  return (last > 0 && 2 * last <= sms) ? last : 0;
+}
+
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
                float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
@@ -1213,11 +1221,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
   constexpr bool kTail = HD == 128 && SLOTS == 2 && SPLIT_P == 2 && !FP8 && !SPLITKV && !CAUSAL;
-  int64_t tail = 0;
-  if (kTail && rc.sms > 0) {
-    const int64_t last = pairs % rc.sms;
-    if (last > 0 && 2 * last <= rc.sms) tail = last;
-  }
+  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms) : 0;
   if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
   const int n_main = static_cast<int>(pairs - tail);
   if (n_main > 0) {
@@ -1499,6 +1503,23 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   RunCtl run;
   if ((rc = enter(&run)) != ATTN_OK) return rc;
   return enqueue_fwd(q, k, v, o, lse, B * H, Nq, Nk, D, scale, causal, static_cast<cudaStream_t>(stream), run);
+}
+
+int attn_fwd_launch_count(int B, int H, int Nq, int Nk, int D, int causal) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || (D != 64 && D != 128)) return -ATTN_EINVAL;
+  if (B == 0 || H == 0 || Nq == 0) return 0;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    ContextState* st = nullptr;
+    const int r = context_state(&st);
+    if (r != ATTN_OK) return -r;
+    sms = st->sms;
+  }
+  if (D != 128 || causal) return 1;
+  const int64_t pairs = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
+  const int64_t tail = tail_pairs(pairs, sms);
+  return (pairs - tail > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);
 }
 
 size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int D, int num_splits) {

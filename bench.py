@@ -312,7 +312,9 @@ def main():
     if fp8:  # V^T workspace, allocated once outside every timed region
         ws_bytes = attn.fp8_workspace_bytes(w.B, w.H, w.Nk, w.D)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    launches_per_step = 2 if (splits > 0 or fp8) else 1
+    # kernels per step: the transpose and the forward (E4M3), the forward and
+    # the merge (split-KV), else what the library reports for the single pass
+    launches_per_step = 2 if (splits > 0 or fp8) else attn.fwd_launch_count(w.B, w.H, w.Nq, w.Nk, w.D, w.causal)
 
     def call():
         """One forward through the C ABI on the launching stream."""

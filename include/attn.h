@@ -98,6 +98,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Nk, int D, float scale, int causal, void* stream);
 
 /*
+ * The number of kernels attn_fwd enqueues for these sizes on the current
+ * device: 1, or 2 for the non-causal D = 128 forward when the query-tile
+ * pairs of a last partial wave that would occupy at most half the SMs run
+ * as a second launch of single-query-tile CTAs (0 when there is nothing to
+ * compute).  For counting launches, e.g. in a benchmark.  Returns
+ * -ATTN_EINVAL for bad sizes, -ATTN_EUNSUPPORTED / -ATTN_ECUDA when the
+ * current device cannot be used.
+ */
+int attn_fwd_launch_count(int B, int H, int Nq, int Nk, int D, int causal);
+
+/*
  * attn_fwd_host -- attn_fwd for tensors in HOST memory: copies Q, K and V
  * to the caller's device buffers, runs the forward and copies O and LSE back,
  * with the three overlapped.  The heads (the flattened B*H) are cut into

@@ -216,3 +216,9 @@ def test_fp8_host_entry_validation_without_device(lib):
     assert f(*(base[:17] + (0.0,) + base[18:]), *ws, 0, None) == attn.ATTN_EINVAL        # q_descale 0
     assert f(*(base[:6] + (A,) + base[7:]), *ws, 0, None) == attn.ATTN_EUNSUPPORTED      # k_dev = q_dev
     assert f(*base, 0, 0, 0, None) == attn.ATTN_EINVAL                                   # no workspace
+
+
+def test_launch_count_argument_checks_without_device(lib):
+    assert attn.fwd_launch_count(1, 4, 128, 128, 96, False) == -attn.ATTN_EINVAL
+    assert attn.fwd_launch_count(1, 4, 128, 0, 128, False) == -attn.ATTN_EINVAL
+    assert attn.fwd_launch_count(0, 4, 128, 128, 128, False) == 0

@@ -59,6 +59,19 @@ def test_edge_shapes(B, H, Nq, Nk, D, causal):
     full_parity(B, H, Nq, Nk, D, causal, seed=1000 + Nq + 7 * Nk + D)
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 80, 300, 300),    # 160 pairs: on 152 SMs the last 8 run as single query tiles, some past Nq
+    (1, 3, 1000, 777),    # 12 pairs, all as single query tiles (an odd key tile count per tile)
+    (2, 40, 512, 129),    # 160 pairs, two key tiles each: warpgroup 1 holds the ragged one
+])
+def test_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk):
+    """Non-causal D=128: the pairs of a last wave that would fill at most half
+    the SMs are re-run as CTAs of one query tile, both warpgroups sharing its
+    key tiles and merging their carriers (every other shape of these tests
+    with few heads takes that path too)."""
+    full_parity(B, H, Nq, Nk, 128, False, seed=500 + H + Nk)
+
+
 @pytest.mark.parametrize("D,causal", [(64, False), (128, True)])
 def test_peaked_scores_small(D, causal):
     """Q, K ~ N(0, 3^2): sharply peaked rows, the running max jumps often."""
@@ -269,3 +282,27 @@ def test_huge_jump_of_the_running_max(causal):
     k[:, :, 200:] += np.float16(8.0)
     v = synth.normal_fp16((B, H, N, D), 1.0, 8, 2)
     _run_and_compare(q, k, v, 1.0 / math.sqrt(D), causal, "huge jump")
+
+
+def test_launch_count_reports_the_single_tile_launch():
+    """attn_fwd_launch_count: two kernels exactly when the non-causal D=128
+    forward re-runs a last partial wave of at most half the SMs as
+    single-query-tile CTAs next to full waves of pairs; one otherwise."""
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def expected(B, H, Nq, D, causal):
+        pairs = B * H * ((Nq + 255) // 256)
+        if D != 128 or causal:
+            return 1
+        last = pairs % sms
+        tail = last if (last > 0 and 2 * last <= sms) else 0
+        return int(pairs - tail > 0) + int(tail > 0)
+
+    for (B, H, Nq, Nk, D, causal) in [(1, 16, 8192, 8192, 128, False), (4, 32, 16384, 16384, 128, False),
+                                      (1, 4, 512, 8192, 128, False), (2, 16, 16384, 16384, 128, True),
+                                      (1, 8, 4096, 4096, 64, False), (1, 80, 300, 300, 128, False)]:
+        assert attn.fwd_launch_count(B, H, Nq, Nk, D, causal) == expected(B, H, Nq, D, causal)
+    assert attn.fwd_launch_count(0, 4, 128, 128, 128, False) == 0
+    assert attn.fwd_launch_count(1, 4, 128, 128, 96, False) == -attn.ATTN_EINVAL
