@@ -53,6 +53,12 @@
 //     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
 //
+//   * Wave quantisation (non-causal fp16 D = 128): when a launch's last
+//     wave of CTAs would occupy at most half the SMs, its pairs run as a
+//     second launch of CTAs that each take one query tile, the two
+//     warpgroups alternating its key tiles and merging their carriers at
+//     the end -- twice the CTAs, half the work each.
+//
 // TMEM (512 columns): at D = 128, S_0/P_0 [0,128), S_1/P_1 [128,256),
 // O_0 [256,384), O_1 [384,512).  At D = 64 three score slots [0,128),
 // [128,256), [256,384) rotate between the two query tiles (so a tile's next

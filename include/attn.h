@@ -79,6 +79,10 @@ enum {
  *   scale  softmax scale, finite and >= 0 (the pages use 1/sqrt(D)).
  *   causal 0: every key is admissible; nonzero: key j masked when j > i.
  *
+ * Enqueues one kernel on `stream`, or two for the non-causal D = 128
+ * forward when the last wave of CTAs would occupy at most half the SMs
+ * (attn_fwd_launch_count tells which).
+ *
  * Key range: the keys one row accumulates -- Nk, or min(Nk, Nq) when causal
  * -- must not exceed ATTN_MAX_KEYS_PER_PASS (2^19), else ATTN_ETOOLONG is
  * returned and nothing is enqueued; attn_fwd_splitkv takes longer rows.
