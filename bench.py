@@ -80,12 +80,23 @@ def gpu_local_cpus(dev_index: int):
     return None
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments and blank-only lines (string literals in
+    these files hold no comment markers)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_digest() -> str:
+    """Digest of the kernel source's code (comments do not count), which
+    keys the recorded ncu traffic to the code it was measured on."""
     h = hashlib.sha256()
     for rel in ("attention_forward_12_gb300/csrc/attn_fwd.cu",
                 "attention_forward_12_gb300/csrc/sm103_primitives.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
