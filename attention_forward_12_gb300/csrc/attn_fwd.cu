@@ -53,7 +53,7 @@
 //     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
 //
-//   * Wave quantisation (non-causal fp16 D = 128): when a launch's last
+//   * Wave quantisation (non-causal fp16): when a launch's last
 //     wave of CTAs would occupy at most half the SMs, its pairs run as a
 //     second launch of CTAs that each take one query tile, the two
 //     warpgroups alternating its key tiles and merging their carriers at
@@ -253,7 +253,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int lane = threadIdx.x & 31;
   // Work of this CTA.  Usually two query tiles of one (batch, head) -- a
   // pair -- each warpgroup taking one of them against every key tile (of the
-  // share, with split-KV).  SINGLE (the non-causal fp16 D = 128 forward):
+  // share, with split-KV).  SINGLE (the non-causal fp16 forward):
   // one query tile, both warpgroups sharing its key range -- warpgroup w
   // takes key tiles w, w + 2, ... -- and merging their two partial results
   // at the end.  The host runs the pairs of a last partial wave that would
@@ -262,7 +262,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // (n_main: the pairs it keeps, in (head, pair) order), and the single-
   // tile launch's CTA b takes query tile b % 2 of pair n_main + b / 2.
   constexpr bool single = SINGLE;
-  static_assert(!SINGLE || (SLOTS == 2 && SPLIT_P == 2 && !FP8 && !SPLITKV && !CAUSAL), "single-tile CTAs");
+  static_assert(!SINGLE || (SLOTS == 2 && !FP8 && !SPLITKV && !CAUSAL), "single-tile CTAs");
   int bh, pair, half = 0;
   if constexpr (SINGLE) {
     const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
@@ -1208,7 +1208,7 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 }
 
 // One forward: the grid of (query-tile pair, head, share) CTAs.  For the
-// non-causal fp16 D = 128 single pass, the pairs of a last partial wave that
+// non-causal fp16 single pass, the pairs of a last partial wave that
 // would occupy at most half the SMs go to a second launch of single-tile
 // CTAs (two per pair, half the work each), which runs as soon as the full
 // waves are done: that wave then takes half as long.
@@ -1226,7 +1226,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
                const RunCtl& rc, float o_scale = 1.0f) {
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
-  constexpr bool kTail = HD == 128 && SLOTS == 2 && SPLIT_P == 2 && !FP8 && !SPLITKV && !CAUSAL;
+  constexpr bool kTail = !FP8 && !SPLITKV && !CAUSAL;
   const int64_t tail = kTail ? tail_pairs(pairs, rc.sms) : 0;
   if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
   const int n_main = static_cast<int>(pairs - tail);
@@ -1236,8 +1236,10 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     if (r != ATTN_OK) return r;
   }
   if constexpr (kTail) {
+    // The single-tile CTAs use two score slots, one per warpgroup, also at
+    // D = 64 (their warpgroups alternate key tiles, so slots need not rotate).
     if (tail > 0)
-      return launch_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, true>(
+      return launch_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, 2, true>(
           mq, mk, mv, o, lse, ws_o, ws_l, dim3(static_cast<unsigned>(2 * tail)), Nq, Nk, sl2, n_main, st, rc,
           o_scale);
   }
@@ -1522,7 +1524,7 @@ int attn_fwd_launch_count(int B, int H, int Nq, int Nk, int D, int causal) {
     if (r != ATTN_OK) return -r;
     sms = st->sms;
   }
-  if (D != 128 || causal) return 1;
+  if (causal) return 1;
   const int64_t pairs = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
   const int64_t tail = tail_pairs(pairs, sms);
   return (pairs - tail > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);

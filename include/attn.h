@@ -79,8 +79,8 @@ enum {
  *   scale  softmax scale, finite and >= 0 (the pages use 1/sqrt(D)).
  *   causal 0: every key is admissible; nonzero: key j masked when j > i.
  *
- * Enqueues one kernel on `stream`, or two for the non-causal D = 128
- * forward when the last wave of CTAs would occupy at most half the SMs
+ * Enqueues one kernel on `stream`, or two for the non-causal forward when
+ * the last wave of CTAs would occupy at most half the SMs
  * (attn_fwd_launch_count tells which).
  *
  * Key range: the keys one row accumulates -- Nk, or min(Nk, Nq) when causal
@@ -103,7 +103,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 /*
  * The number of kernels attn_fwd enqueues for these sizes on the current
- * device: 1, or 2 for the non-causal D = 128 forward when the query-tile
+ * device: 1, or 2 for the non-causal forward when the query-tile
  * pairs of a last partial wave that would occupy at most half the SMs run
  * as a second launch of single-query-tile CTAs (0 when there is nothing to
  * compute).  For counting launches, e.g. in a benchmark.  Returns

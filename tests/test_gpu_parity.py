@@ -59,17 +59,19 @@ def test_edge_shapes(B, H, Nq, Nk, D, causal):
     full_parity(B, H, Nq, Nk, D, causal, seed=1000 + Nq + 7 * Nk + D)
 
 
-@pytest.mark.parametrize("B,H,Nq,Nk", [
-    (1, 80, 300, 300),    # 160 pairs: on 152 SMs the last 8 run as single query tiles, some past Nq
-    (1, 3, 1000, 777),    # 12 pairs, all as single query tiles (an odd key tile count per tile)
-    (2, 40, 512, 129),    # 160 pairs, two key tiles each: warpgroup 1 holds the ragged one
+@pytest.mark.parametrize("B,H,Nq,Nk,D", [
+    (1, 80, 300, 300, 128),   # 160 pairs: on 152 SMs the last 8 run as single query tiles, some past Nq
+    (1, 3, 1000, 777, 128),   # 12 pairs, all as single query tiles (an odd key tile count per tile)
+    (2, 40, 512, 129, 128),   # 160 pairs, two key tiles each: warpgroup 1 holds the ragged one
+    (1, 80, 300, 300, 64),    # the same at D=64 (single-tile CTAs with two score slots)
+    (1, 3, 1000, 777, 64),
 ])
-def test_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk):
-    """Non-causal D=128: the pairs of a last wave that would fill at most half
-    the SMs are re-run as CTAs of one query tile, both warpgroups sharing its
-    key tiles and merging their carriers (every other shape of these tests
-    with few heads takes that path too)."""
-    full_parity(B, H, Nq, Nk, 128, False, seed=500 + H + Nk)
+def test_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk, D):
+    """Non-causal: the pairs of a last wave that would fill at most half the
+    SMs are re-run as CTAs of one query tile, both warpgroups sharing its key
+    tiles and merging their carriers (every other shape of these tests with
+    few heads takes that path too)."""
+    full_parity(B, H, Nq, Nk, D, False, seed=500 + H + Nk + D)
 
 
 @pytest.mark.parametrize("D,causal", [(64, False), (128, True)])
@@ -285,7 +287,7 @@ def test_huge_jump_of_the_running_max(causal):
 
 
 def test_launch_count_reports_the_single_tile_launch():
-    """attn_fwd_launch_count: two kernels exactly when the non-causal D=128
+    """attn_fwd_launch_count: two kernels exactly when the non-causal
     forward re-runs a last partial wave of at most half the SMs as
     single-query-tile CTAs next to full waves of pairs; one otherwise."""
     torch = torch_cuda()
@@ -294,7 +296,7 @@ def test_launch_count_reports_the_single_tile_launch():
 
     def expected(B, H, Nq, D, causal):
         pairs = B * H * ((Nq + 255) // 256)
-        if D != 128 or causal:
+        if causal:
             return 1
         last = pairs % sms
         tail = last if (last > 0 and 2 * last <= sms) else 0
