@@ -1213,11 +1213,16 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 // CTAs (two per pair, half the work each), which runs as soon as the full
 // waves are done: that wave then takes half as long.
 // Pairs of the last partial wave that go to single-tile CTAs: all of the
-// last wave's pairs when it would occupy at most half of the `sms` SMs.
-int64_t tail_pairs(int64_t pairs, int sms) {
+// last wave's pairs when it would occupy at most half of the `sms` SMs --
+// and, when full waves of pairs come first, only if each query tile has at
+// least 16 key tiles: the second launch then waits for the full waves and
+// costs a few microseconds, more than half a wave of short CTAs saves.
+int64_t tail_pairs(int64_t pairs, int sms, int key_tiles) {
   if (sms <= 0) return 0;
   const int64_t last = pairs % sms;
-  return (last > 0 && 2 * last <= sms) ? last : 0;
+  if (last == 0 || 2 * last > sms) return 0;
+  if (last < pairs && key_tiles < 16) return 0;
+  return last;
 }
 
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
@@ -1227,7 +1232,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
   constexpr bool kTail = !FP8 && !SPLITKV && !CAUSAL;
-  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms) : 0;
+  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms, (Nk + kBlockN - 1) / kBlockN) : 0;
   if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
   const int n_main = static_cast<int>(pairs - tail);
   if (n_main > 0) {
@@ -1526,7 +1531,7 @@ int attn_fwd_launch_count(int B, int H, int Nq, int Nk, int D, int causal) {
   }
   if (causal) return 1;
   const int64_t pairs = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
-  const int64_t tail = tail_pairs(pairs, sms);
+  const int64_t tail = tail_pairs(pairs, sms, (Nk + kBlockN - 1) / kBlockN);
   return (pairs - tail > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);
 }
 
