@@ -53,11 +53,11 @@
 //     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
 //
-//   * Wave quantisation (non-causal fp16): when a launch's last
-//     wave of CTAs would occupy at most half the SMs, its pairs run as a
-//     second launch of CTAs that each take one query tile, the two
-//     warpgroups alternating its key tiles and merging their carriers at
-//     the end -- twice the CTAs, half the work each.
+//   * Wave quantisation (non-causal single pass, fp16 and E4M3): when a
+//     launch's last wave of CTAs would occupy at most half the SMs, its
+//     pairs run as a second launch of CTAs that each take one query tile,
+//     the two warpgroups alternating its key tiles and merging their
+//     carriers at the end -- twice the CTAs, half the work each.
 //
 // TMEM (512 columns): at D = 128, S_0/P_0 [0,128), S_1/P_1 [128,256),
 // O_0 [256,384), O_1 [384,512).  At D = 64 three score slots [0,128),
@@ -253,7 +253,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int lane = threadIdx.x & 31;
   // Work of this CTA.  Usually two query tiles of one (batch, head) -- a
   // pair -- each warpgroup taking one of them against every key tile (of the
-  // share, with split-KV).  SINGLE (the non-causal fp16 forward):
+  // share, with split-KV).  SINGLE (the non-causal single pass):
   // one query tile, both warpgroups sharing its key range -- warpgroup w
   // takes key tiles w, w + 2, ... -- and merging their two partial results
   // at the end.  The host runs the pairs of a last partial wave that would
@@ -262,7 +262,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // (n_main: the pairs it keeps, in (head, pair) order), and the single-
   // tile launch's CTA b takes query tile b % 2 of pair n_main + b / 2.
   constexpr bool single = SINGLE;
-  static_assert(!SINGLE || (SLOTS == 2 && !FP8 && !SPLITKV && !CAUSAL), "single-tile CTAs");
+  static_assert(!SINGLE || (SLOTS == 2 && !SPLITKV && !CAUSAL), "single-tile CTAs");
   int bh, pair, half = 0;
   if constexpr (SINGLE) {
     const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
@@ -749,7 +749,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float a0 = ex2_approx(m0 - m);
         const float a1 = nkv1 > 0 ? ex2_approx(m1 - m) : 0.f;
         const float d = a0 * x_d[row] + a1 * x_d[kBlockM + row];
-        const float inv = 1.f / d;
+        const float inv = o_scale / d;  // o_scale: the E4M3 kernel's V descale, else 1
         const float2 c0 = make_float2(a0 * inv, a0 * inv), c1 = make_float2(a1 * inv, a1 * inv);
         const uint32_t tO0 = tmem + kOCol + lane_off, tO1 = tmem + kOCol + kOStride + lane_off;
         __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
@@ -1208,7 +1208,7 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 }
 
 // One forward: the grid of (query-tile pair, head, share) CTAs.  For the
-// non-causal fp16 single pass, the pairs of a last partial wave that
+// non-causal single pass (fp16 or E4M3), the pairs of a last partial wave that
 // would occupy at most half the SMs go to a second launch of single-tile
 // CTAs (two per pair, half the work each), which runs as soon as the full
 // waves are done: that wave then takes half as long.
@@ -1231,7 +1231,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
                const RunCtl& rc, float o_scale = 1.0f) {
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
-  constexpr bool kTail = !FP8 && !SPLITKV && !CAUSAL;
+  constexpr bool kTail = !SPLITKV && !CAUSAL;
   const int64_t tail = kTail ? tail_pairs(pairs, rc.sms, (Nk + kBlockN - 1) / kBlockN) : 0;
   if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
   const int n_main = static_cast<int>(pairs - tail);

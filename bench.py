@@ -323,9 +323,12 @@ def main():
     if fp8:  # V^T workspace, allocated once outside every timed region
         ws_bytes = attn.fp8_workspace_bytes(w.B, w.H, w.Nk, w.D)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    # kernels per step: the transpose and the forward (E4M3), the forward and
-    # the merge (split-KV), else what the library reports for the single pass
-    launches_per_step = 2 if (splits > 0 or fp8) else attn.fwd_launch_count(w.B, w.H, w.Nq, w.Nk, w.D, w.causal)
+    # kernels per step: the forward and the merge (split-KV), else what the
+    # library reports for the single pass, plus the V transpose for E4M3
+    if splits > 0:
+        launches_per_step = 2
+    else:
+        launches_per_step = attn.fwd_launch_count(w.B, w.H, w.Nq, w.Nk, w.D, w.causal) + (1 if fp8 else 0)
 
     def call():
         """One forward through the C ABI on the launching stream."""

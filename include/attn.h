@@ -258,7 +258,10 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
  *          Two calls that share a workspace must not run concurrently.
  *   B, H, Nq, Nk, scale, causal, stream: as attn_fwd.  D must be 128.
  *
- * Enqueues two kernels (the transpose, then the forward) on `stream`.
+ * Enqueues the transpose, then the forward's kernels, on `stream`: one
+ * more than attn_fwd_launch_count(B, H, Nq, Nk, 128, causal), the forward
+ * following the same rule as attn_fwd's on when its last partial wave runs
+ * as a second launch of single-query-tile CTAs.
  * Errors as attn_fwd, plus ATTN_EINVAL for a descale that is not finite and
  * positive or a missing / too small workspace, ATTN_EUNSUPPORTED for D != 128
  * or a misaligned or overlapping workspace.

@@ -96,6 +96,24 @@ def test_fp8_matches_oracle(B, H, Nq, Nk, causal, sqk, seed):
     check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, causal, label=f"[{B},{H},{Nq},{Nk}] causal={causal}")
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk,heads", [
+    # 160 pairs: on 152 SMs the last 8 (heads 76-79) run as single query tiles
+    (1, 80, 300, 2100, (0, 1, 37, 75, 76, 77, 78, 79)),
+    # 160 pairs with 17 key tiles each: warpgroup 0 of a single-tile CTA holds the ragged one
+    (2, 40, 512, 2049, (0, 38, 39, 76, 77, 78, 79)),
+])
+def test_fp8_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk, heads):
+    """Non-causal E4M3: the pairs of a last wave that would fill at most half
+    the SMs run as CTAs of one query tile whose warpgroups alternate key
+    tiles and merge their carriers (with the V descale applied there).
+    Checked on every row of a few heads, including all of the single-tile
+    ones; the flattened head index is b * H + h."""
+    q8, k8, v8 = synth.make_qkv_e4m3(B, H, Nq, Nk, 128, seed=4300 + H, sigma_qk=2.0)
+    o, lse = run_fp8(q8, k8, v8, 128 ** -0.5, False, vd=0.5)
+    rows = np.concatenate([np.arange(bh * Nq, (bh + 1) * Nq) for bh in heads])
+    check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, False, vd=0.5, rows=rows, label=f"[{B},{H},{Nq},{Nk}] partial wave")
+
+
 def test_fp8_descales():
     q8, k8, v8 = synth.make_qkv_e4m3(1, 2, 256, 2048, 128, seed=4100, sigma_qk=2.0)
     args = dict(qd=0.5, kd=3.0, vd=0.25)
