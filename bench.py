@@ -239,6 +239,15 @@ def run_reference(args, w):
     return 0
 
 
+def percentile(xs, pct):
+    """Linear-interpolated percentile of a non-empty list (numpy's default rule)."""
+    ys = sorted(xs)
+    x = (len(ys) - 1) * pct / 100.0
+    lo = int(x)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (x - lo)
+
+
 def config_of(w, splits=0):
     return {"workload": w.name, "split_kv_shares": splits, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
             "causal": w.causal, "scale": w.scale, "sigma_qk": w.sigma_qk, "sigma_v": w.sigma_v,
@@ -529,6 +538,9 @@ def main():
         "data": "synthetic", "config": config_of(w, splits), "parallelism": f"replicas x{world} (independent problems)",
         "gpu_launches": args.steps * launches_per_step, "roofline": roofline, "clocks": clk.summary(),
         "e2e": e2e, "cpu_baseline": cpu,
+        # per-call device time of this rank: each step's own pair of events
+        "call_us": {"median": 1e3 * statistics.median(kernel_ms), "p10": 1e3 * percentile(kernel_ms, 10),
+                    "p90": 1e3 * percentile(kernel_ms, 90), "n": len(kernel_ms)},
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

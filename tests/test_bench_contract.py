@@ -33,3 +33,16 @@ def test_reference_arm_prints_one_contract_line():
 
 def test_reference_arm_other_ranks_stay_silent():
     assert _run({"RANK": "1"}) == []
+
+
+def test_percentile_matches_numpy():
+    """bench.percentile (the per-call p10 / p90 of the bench line) against
+    numpy's linear-interpolation rule."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    rng = np.random.default_rng(7)
+    for n in (1, 2, 5, 20):
+        xs = list(rng.random(n))
+        for pct in (0, 10, 50, 90, 100):
+            assert abs(bench.percentile(xs, pct) - float(np.percentile(xs, pct))) < 1e-12
