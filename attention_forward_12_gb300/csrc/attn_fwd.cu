@@ -102,19 +102,26 @@ constexpr int kEmu128 = 0;
 // the polynomial's device code runs inside the forward under test.
 constexpr int kDebugEmu = 4;
 
-template <int HD, int NS, bool FP8 = false>
+template <int HD, int NS, bool FP8 = false, int QT = 2>
 struct Layout {
   static constexpr int kElem = FP8 ? 1 : 2;                   // bytes per element
   static constexpr int kChunks = HD * kElem / 128;            // 128-byte column blocks per row
   static constexpr int kChunkElems = 128 / kElem;
   static constexpr uint32_t kTileBytes = kBlockM * HD * kElem;  // one Q, K or V tile
-  // q_full, k/v full/empty[NS], s_full/p_half/p_full[3] (one per TMEM score
-  // slot), o_done[4], drain, xchg; then the TMEM address, the abort flag and
-  // the last loads per stage, and the (m, d) exchange of a single-tile CTA
+  // QT query tiles, then NS K and NS V stages; q_full, k/v full/empty[NS],
+  // s_full/p_half/p_full[3] (one per TMEM score slot), o_done[4], drain,
+  // xchg; then the TMEM address, the abort flag and the last loads per stage
   static constexpr int kBars = 1 + 4 * NS + 3 * 3 + 4 + 1 + 1;
-  static constexpr size_t kXchgBytes = 2 * 2 * kBlockM * sizeof(float);
-  static constexpr size_t kSmem = 1024 + kTileBytes * (2 + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8 + kXchgBytes;
+  static constexpr size_t kSmem = 1024 + kTileBytes * (QT + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
 };
+
+// K/V ring depth of the single-tile CTAs.  They hold one query tile, so at
+// fp16 D = 128 the ring takes the second tile's space and grows from 2 to 3
+// stages of 64 KB: a V stage is then free a tile earlier, and the loads of
+// the tile after next no longer wait for the last product.  The 16 KB-tile
+// kernels (D = 64, E4M3) keep the pairs' 4 stages: 6 measured no faster.
+template <int HD, bool FP8>
+constexpr int single_stages() { return (HD == 128 && !FP8) ? 3 : 4; }
 
 // Key tiles query tile w of the CTA visits (0 if the tile lies past Nq).
 template <bool CAUSAL>
@@ -221,14 +228,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 int drop_tile, int n_main) {
   static_assert(!FP8 || HD == 128, "the E4M3 kernel is built for D = 128 only");
   static_assert(SPLIT_P == 0 || SPLIT_P == 2, "P released whole (0) or in two halves (2)");
-  using L = Layout<HD, NS, FP8>;
+  constexpr int QT = SINGLE ? 1 : 2;  // query tiles held in shared memory
+  using L = Layout<HD, NS, FP8, QT>;
   constexpr uint32_t TB = L::kTileBytes;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* sQ = sm;                 // 2 tiles
-  uint8_t* sK = sQ + 2 * TB;        // NS tiles
+  uint8_t* sQ = sm;                 // QT tiles
+  uint8_t* sK = sQ + QT * TB;       // NS tiles
   uint8_t* sV = sK + NS * TB;       // NS tiles
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sV + NS * TB);
   uint64_t* k_full = q_full + 1;
@@ -246,8 +254,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* last_k = abort_flag + 1;     // [NS] last tile loaded per stage (abort drain)
   int* last_v = last_k + NS;
-  float* x_m = reinterpret_cast<float*>(last_v + NS);  // [2][128] single-tile CTA: m per warpgroup and row
-  float* x_d = x_m + 2 * kBlockM;                      // [2][128] d per warpgroup and row
+  // Single-tile CTA: the (m, d) exchange of the two warpgroups, in the
+  // query tile's buffer, which is free once every product has completed.
+  float* x_m = reinterpret_cast<float*>(sQ);  // [2][128] m per warpgroup and row
+  float* x_d = x_m + 2 * kBlockM;             // [2][128] d per warpgroup and row
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -429,8 +439,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // those of fp16.)
     constexpr uint32_t kIdescPV = idesc_f16_f32(kBlockM, HD, false, !FP8);
     const uint64_t dQ = smem_desc(base, 16, 1024);
-    const uint64_t dK = smem_desc(base + 2 * TB, 16, 1024);
-    const uint64_t dV = smem_desc(base + (2 + NS) * TB, FP8 ? 16u : kChunkBytes, 1024);
+    const uint64_t dK = smem_desc(base + QT * TB, 16, 1024);
+    const uint64_t dV = smem_desc(base + (QT + NS) * TB, FP8 ? 16u : kChunkBytes, 1024);
     constexpr int kQkSteps = HD * L::kElem / 32;       // 32 bytes of D per product
     constexpr int kPvSteps = kBlockN * L::kElem / 32;  // 32 bytes of keys per product
     // S_w = Q_w K^T of stage s: both operands K-major, 128B swizzle; the
@@ -737,7 +747,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // (a0 d0 + a1 d1).  The (m, d) pairs go through shared memory; then
       // warpgroup w writes columns [64 w, 64 w + 64) of every row, reading
       // them from both O accumulators (any warp may read the TMEM lanes of
-      // its sub-partition, whichever warpgroup accumulated them).
+      // its sub-partition, whichever warpgroup accumulated them).  The
+      // exchange overwrites the query tile, so each warpgroup first sees
+      // both warpgroups' last products complete: their commits follow the
+      // issue of every Q K^T (a warpgroup without a key tile has not waited
+      // for any yet).
+      if (nkv1 > 0 && wg == 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[1], (nkv1 - 1) & 1, wc, ATTN_ETIMEOUT));
+      if (wg == 1)
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[0], (nkv0 - 1) & 1, wc, ATTN_ETIMEOUT));
+    }
+    if (single && ok) {
       x_m[wg * kBlockM + row] = m_ref;
       x_d[wg * kBlockM + row] = dsum;
       mbar_arrive(xchg);
@@ -1176,7 +1196,7 @@ template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool 
 int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
                   float* ws_o, float* ws_l, dim3 grid, int Nq, int Nk, float sl2, int n_main, cudaStream_t st,
                   const RunCtl& rc, float o_scale) {
-  using L = Layout<HD, NS, FP8>;
+  using L = Layout<HD, NS, FP8, SINGLE ? 1 : 2>;
   auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, SINGLE>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
   // The shared-memory attribute is set on the first launch on each device
@@ -1244,7 +1264,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     // The single-tile CTAs use two score slots, one per warpgroup, also at
     // D = 64 (their warpgroups alternate key tiles, so slots need not rotate).
     if (tail > 0)
-      return launch_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, 2, true>(
+      return launch_kernel<HD, CAUSAL, single_stages<HD, FP8>(), SPLIT_P, EMU, SPLITKV, FP8, 2, true>(
           mq, mk, mv, o, lse, ws_o, ws_l, dim3(static_cast<unsigned>(2 * tail)), Nq, Nk, sl2, n_main, st, rc,
           o_scale);
   }
