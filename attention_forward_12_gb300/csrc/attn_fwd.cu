@@ -48,7 +48,8 @@
 //     otherwise p is taken against the stale reference, which is exact
 //     because p, d and o share it (the conditional rescale the page credits
 //     to FlashAttention-4 in "Relationship to FA-3 and FA-4").  At the end the
-//     warpgroup normalises O_w by d and writes fp16 O and fp32 LSE.
+//     warpgroup normalises O_w by d and writes fp16 O (staged in its query
+//     tile's shared-memory buffer and stored with TMA) and fp32 LSE.
 //   * Causal (key j masked when j > i): each query tile visits only the key
 //     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
@@ -110,8 +111,9 @@ struct Layout {
   static constexpr uint32_t kTileBytes = kBlockM * HD * kElem;  // one Q, K or V tile
   // QT query tiles, then NS K and NS V stages; q_full, k/v full/empty[NS],
   // s_full/p_half/p_full[3] (one per TMEM score slot), o_done[4], drain,
-  // xchg; then the TMEM address, the abort flag and the last loads per stage
-  static constexpr int kBars = 1 + 4 * NS + 3 * 3 + 4 + 1 + 1;
+  // xchg, o_staged[2]; then the TMEM address, the abort flag and the last
+  // loads per stage
+  static constexpr int kBars = 1 + 4 * NS + 3 * 3 + 4 + 1 + 1 + 2;
   static constexpr size_t kSmem = 1024 + kTileBytes * (QT + 2 * NS) + kBars * 8 + 8 + 8 + NS * 8;
 };
 
@@ -222,7 +224,8 @@ __device__ int g_attn_status;
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8, int SLOTS, bool SINGLE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, __half* __restrict__ out,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                __half* __restrict__ out,
                 float* __restrict__ lse, float* __restrict__ ws_o, float* __restrict__ ws_l, int Nq, int Nk,
                 float sl2, float o_scale, int* status_host, uint64_t timeout_ns,
                 int drop_tile, int n_main) {
@@ -250,7 +253,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                     // product; SLOTS = 3: [2w + (j & 1)], one phase per two
   uint64_t* drain = o_done + 4;     // abort path only
   uint64_t* xchg = drain + 1;       // single-tile CTA: both warpgroups' (m, d) written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg + 1);
+  uint64_t* o_staged = xchg + 1;    // [2] fp16 O tile w staged in shared memory for its TMA store
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_staged + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* last_k = abort_flag + 1;     // [NS] last tile loaded per stage (abort drain)
   int* last_v = last_k + NS;
@@ -344,6 +348,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int b = 0; b < 4; ++b) mbar_init(&o_done[b], 1);
     mbar_init(drain, 1);
     mbar_init(xchg, 2 * kBlockM);
+    mbar_init(&o_staged[0], kBlockM);
+    mbar_init(&o_staged[1], kBlockM);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -807,22 +813,61 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       const float inv = o_scale / dsum;  // o_scale: the E4M3 kernel's V descale, else 1
       const float2 iv = make_float2(inv, inv);
-      __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
+      if constexpr (!FP8) {
+        // O / d as fp16 into this warpgroup's query-tile buffer (free: every
+        // Q_w K^T was issued before the last O_w += P_w V, whose completion
+        // was just seen), in the 128B-swizzled layout of the TMA box --
+        // 16-byte unit u of row r at u ^ (r mod 8) -- then one thread
+        // stores the tile with TMA; rows past Nq lie outside the tensor and
+        // are not written.
+        uint8_t* so = sQ + wg * TB;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(tO + c * 32, orr);
-        tmem_ld_wait(orr);
-        if (i < Nq) {
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + c * 32, orr);
+          tmem_ld_wait(orr);
           uint32_t h[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1])), iv);
             h[e] = pack_half2(v.x, v.y);
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          uint8_t* srow = so + (c >> 1) * kChunkBytes + row * 128;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) {
+            const int u = (c & 1) * 4 + e;
+            *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) =
+                make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&o_staged[wg]);
+        if (row == 0) {
+          if (mbar_wait(&o_staged[wg], 0, wc, ATTN_ETIMEOUT)) {
+#pragma unroll
+            for (int k = 0; k < HD / 64; ++k) tma_store_3d(&tmO, so + k * kChunkBytes, k * 64, rw, bh);
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+        }
+      } else {
+        __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + c * 32, orr);
+          tmem_ld_wait(orr);
+          if (i < Nq) {
+            uint32_t h[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1])), iv);
+              h[e] = pack_half2(v.x, v.y);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+          }
         }
       }
       if (lse != nullptr && i < Nq)
@@ -1193,7 +1238,8 @@ int enter(RunCtl* rc, bool want_noalloc = false) {
 // ------------------------------------------------------------ launches
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2,
           bool SINGLE = false>
-int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
+int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+                  void* o, float* lse,
                   float* ws_o, float* ws_l, dim3 grid, int Nq, int Nk, float sl2, int n_main, cudaStream_t st,
                   const RunCtl& rc, float o_scale) {
   using L = Layout<HD, NS, FP8, SINGLE ? 1 : 2>;
@@ -1212,7 +1258,7 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
       return ATTN_ECUDA;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
+  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, mo, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
                                          o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
   if (cudaGetLastError() == cudaSuccess) return ATTN_OK;
   // A context reset (cudaDeviceReset) drops the attribute: set it again and
@@ -1222,7 +1268,7 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
       cudaSuccess)
     return ATTN_ECUDA;
   attr_set.fetch_or(bit, std::memory_order_release);
-  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
+  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, mo, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
                                          o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
@@ -1246,7 +1292,8 @@ int64_t tail_pairs(int64_t pairs, int sms, int key_tiles) {
 }
 
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
-int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* o, float* lse,
+int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+               void* o, float* lse,
                float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits, cudaStream_t st,
                const RunCtl& rc, float o_scale = 1.0f) {
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
@@ -1257,7 +1304,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const int n_main = static_cast<int>(pairs - tail);
   if (n_main > 0) {
     const int r = launch_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, false>(
-        mq, mk, mv, o, lse, ws_o, ws_l, dim3(n_pairs, BH, splits), Nq, Nk, sl2, n_main, st, rc, o_scale);
+        mq, mk, mv, mo, o, lse, ws_o, ws_l, dim3(n_pairs, BH, splits), Nq, Nk, sl2, n_main, st, rc, o_scale);
     if (r != ATTN_OK) return r;
   }
   if constexpr (kTail) {
@@ -1265,7 +1312,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     // D = 64 (their warpgroups alternate key tiles, so slots need not rotate).
     if (tail > 0)
       return launch_kernel<HD, CAUSAL, single_stages<HD, FP8>(), SPLIT_P, EMU, SPLITKV, FP8, 2, true>(
-          mq, mk, mv, o, lse, ws_o, ws_l, dim3(static_cast<unsigned>(2 * tail)), Nq, Nk, sl2, n_main, st, rc,
+          mq, mk, mv, mo, o, lse, ws_o, ws_l, dim3(static_cast<unsigned>(2 * tail)), Nq, Nk, sl2, n_main, st, rc,
           o_scale);
   }
   return ATTN_OK;
@@ -1276,16 +1323,16 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
 // exponentials in EMU on the FMA-pipe polynomial (0 = none).
 template <bool SPLITKV, int EMU64 = kEmu64, int EMU128 = kEmu128>
 int dispatch_fwd(int D, int causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                 void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
+                 const CUtensorMap& mo, void* o, float* lse, float* ws_o, float* ws_l, int BH, int Nq, int Nk, float sl2, int splits,
                  cudaStream_t st, const RunCtl& rc) {
   if (D == 64)
-    return causal ? launch_fwd<64, true, 4, 0, EMU64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+    return causal ? launch_fwd<64, true, 4, 0, EMU64, SPLITKV, false, 3>(mq, mk, mv, mo, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                          sl2, splits, st, rc)
-                  : launch_fwd<64, false, 4, 0, EMU64, SPLITKV, false, 3>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk,
+                  : launch_fwd<64, false, 4, 0, EMU64, SPLITKV, false, 3>(mq, mk, mv, mo, o, lse, ws_o, ws_l, BH, Nq, Nk,
                                                                           sl2, splits, st, rc);
-  return causal ? launch_fwd<128, true, 2, 2, EMU128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+  return causal ? launch_fwd<128, true, 2, 2, EMU128, SPLITKV>(mq, mk, mv, mo, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
                                                                splits, st, rc)
-                : launch_fwd<128, false, 2, 2, EMU128, SPLITKV>(mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
+                : launch_fwd<128, false, 2, 2, EMU128, SPLITKV>(mq, mk, mv, mo, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2,
                                                                 splits, st, rc);
 }
 
@@ -1364,7 +1411,8 @@ int enqueue_splitkv(const void* q, const void* k, const void* v, void* o, float*
   const size_t rows = static_cast<size_t>(BH) * Nq;
   float* ws_o = static_cast<float*>(workspace);
   float* ws_l = ws_o + static_cast<size_t>(num_splits) * rows * D;
-  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st, rc);
+  // (the split-KV parts write fp32 carriers, not O: the O map is unused)
+  const int r = dispatch_fwd<true>(D, causal, mq, mk, mv, mq, o, lse, ws_o, ws_l, BH, Nq, Nk, sl2, num_splits, st, rc);
   if (r != ATTN_OK) return r;
   return D == 64 ? launch_merge<64>(ws_o, ws_l, o, lse, rows, num_splits, st)
                  : launch_merge<128>(ws_o, ws_l, o, lse, rows, num_splits, st);
@@ -1503,11 +1551,12 @@ int enqueue_fp8(const void* q, const void* k, const void* v, void* o, float* lse
     return ATTN_ECUDA;
   attn_fp8_transpose_v_kernel<<<dim3((Nk + 127) / 128, nb), 256, 0, st>>>(vc, wc, Nk, ldk);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ECUDA;
+  // (the E4M3 forward writes O from registers: its O map argument is unused)
   __half* oc = static_cast<__half*>(o) + qo;
   float* lc = lse ? lse + static_cast<size_t>(h0) * Nq : nullptr;
-  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
+  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, mq, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
                                                              1, st, rc, v_descale)
-                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
+                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, mq, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
                                                               1, st, rc, v_descale);
 }
 
@@ -1515,12 +1564,13 @@ int enqueue_fp8(const void* q, const void* k, const void* v, void* o, float* lse
 template <int EMU64 = kEmu64, int EMU128 = kEmu128>
 int enqueue_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Nq, int Nk, int D,
                 float scale, int causal, cudaStream_t st, const RunCtl& rc) {
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D))
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, q, BH, Nq, D) || !make_map(&mk, k, BH, Nk, D) || !make_map(&mv, v, BH, Nk, D) ||
+      !make_map(&mo, o, BH, Nq, D))
     return ATTN_ECUDA;
   const float sl2 = scale * 1.4426950408889634f;
-  return dispatch_fwd<false, EMU64, EMU128>(D, causal, mq, mk, mv, o, lse, nullptr, nullptr, BH, Nq, Nk, sl2, 1, st,
-                                            rc);
+  return dispatch_fwd<false, EMU64, EMU128>(D, causal, mq, mk, mv, mo, o, lse, nullptr, nullptr, BH, Nq, Nk, sl2, 1,
+                                            st, rc);
 }
 
 }  // namespace

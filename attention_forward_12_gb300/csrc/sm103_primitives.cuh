@@ -1,6 +1,7 @@
 // sm103_primitives.cuh -- inline-PTX building blocks for the sm_103a
-// attention forward: mbarriers with bounded waits, TMA tile loads, and the
-// fifth-generation tensor core (tcgen05.mma with TMEM accumulators).
+// attention forward: mbarriers with bounded waits, TMA tile loads and
+// stores, and the fifth-generation tensor core (tcgen05.mma with TMEM
+// accumulators).
 //
 // Everything here is written from the PTX ISA's descriptions of these
 // instructions.  The encodings used:
@@ -126,6 +127,29 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
         "r"(smem_u32(bar))
       : "memory");
+}
+
+// 3-D tiled store of one box from shared memory (bulk async-group
+// completion).  Elements of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk group of this thread has finished
+// reading its shared-memory source, so the CTA may exit and its shared
+// memory go; the global writes complete on their own.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMEM
