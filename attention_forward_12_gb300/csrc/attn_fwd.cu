@@ -778,7 +778,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float inv = o_scale / d;  // o_scale: the E4M3 kernel's V descale, else 1
         const float2 c0 = make_float2(a0 * inv, a0 * inv), c1 = make_float2(a1 * inv, a1 * inv);
         const uint32_t tO0 = tmem + kOCol + lane_off, tO1 = tmem + kOCol + kOStride + lane_off;
-        __half* orow = out + (static_cast<size_t>(bh) * Nq + i) * HD;
+        // O as fp16 into the first K/V stages (free: every product has
+        // completed), in the 128B-swizzled layout of the 64-column TMA box:
+        // at D = 128 warpgroup w fills box w, at D = 64 the two warpgroups
+        // fill the halves of one box.  Rows past Nq are not stored.
+        uint8_t* so = sK;
 #pragma unroll
         for (int cc = 0; cc < HD / 64; ++cc) {
           const int c = wg * (HD / 64) + cc;  // this warpgroup's 32-column chunks
@@ -792,17 +796,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
             for (int e = 0; e < 32; ++e) o1[e] = 0u;
           }
-          if (i < Nq) {
-            uint32_t h[16];
+          uint32_t h[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float2 v = __ffma2_rn(make_float2(__uint_as_float(o1[2 * e]), __uint_as_float(o1[2 * e + 1])), c1,
-                                          __fmul2_rn(make_float2(__uint_as_float(o0[2 * e]), __uint_as_float(o0[2 * e + 1])), c0));
-              h[e] = pack_half2(v.x, v.y);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int e = 0; e < 16; ++e) {
+            const float2 v = __ffma2_rn(make_float2(__uint_as_float(o1[2 * e]), __uint_as_float(o1[2 * e + 1])), c1,
+                                        __fmul2_rn(make_float2(__uint_as_float(o0[2 * e]), __uint_as_float(o0[2 * e + 1])), c0));
+            h[e] = pack_half2(v.x, v.y);
+          }
+          uint8_t* srow = so + (c >> 1) * kChunkBytes + row * 128;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) {
+            const int u = (c & 1) * 4 + e;
+            *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) =
+                make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&o_staged[wg]);
+        if (row == 0 && (HD == 128 || wg == 0)) {
+          bool staged = mbar_wait(&o_staged[wg], 0, wc, ATTN_ETIMEOUT);
+          if (HD == 64 && staged) staged = mbar_wait(&o_staged[1], 0, wc, ATTN_ETIMEOUT);
+          if (staged) {
+            tma_store_3d(&tmO, so + wg * kChunkBytes, 64 * wg, rw, bh);
+            bulk_commit_group();
+            bulk_wait_read_all();
           }
         }
         if (wg == 0 && lse != nullptr && i < Nq)
@@ -1545,18 +1562,17 @@ int enqueue_fp8(const void* q, const void* k, const void* v, void* o, float* lse
   const uint8_t* kc = static_cast<const uint8_t*>(k) + ko;
   const uint8_t* vc = static_cast<const uint8_t*>(v) + ko;
   uint8_t* wc = static_cast<uint8_t*>(workspace) + wo;
-  CUtensorMap mq, mk, mv;
+  __half* oc = static_cast<__half*>(o) + qo;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map_u8(&mq, qc, nb, Nq, D, D) || !make_map_u8(&mk, kc, nb, Nk, D, D) ||
-      !make_map_u8(&mv, wc, nb, D, Nk, ldk))
+      !make_map_u8(&mv, wc, nb, D, Nk, ldk) || !make_map(&mo, oc, nb, Nq, D))
     return ATTN_ECUDA;
   attn_fp8_transpose_v_kernel<<<dim3((Nk + 127) / 128, nb), 256, 0, st>>>(vc, wc, Nk, ldk);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ECUDA;
-  // (the E4M3 forward writes O from registers: its O map argument is unused)
-  __half* oc = static_cast<__half*>(o) + qo;
   float* lc = lse ? lse + static_cast<size_t>(h0) * Nq : nullptr;
-  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, mq, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
+  return causal ? launch_fwd<128, true, 4, 0, 0, false, true>(mq, mk, mv, mo, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
                                                              1, st, rc, v_descale)
-                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, mq, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
+                : launch_fwd<128, false, 4, 0, 0, false, true>(mq, mk, mv, mo, oc, lc, nullptr, nullptr, nb, Nq, Nk, sl2,
                                                               1, st, rc, v_descale);
 }
 
