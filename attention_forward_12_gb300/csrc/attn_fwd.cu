@@ -751,10 +751,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // the same 128 rows: (m_w, d_w) in registers, O_w in TMEM.  The carrier
       // merge: m = max(m0, m1), a_w = 2^(m_w - m), O = (a0 O0 + a1 O1) /
       // (a0 d0 + a1 d1).  The (m, d) pairs go through shared memory; then
-      // warpgroup w writes columns [64 w, 64 w + 64) of every row, reading
-      // them from both O accumulators (any warp may read the TMEM lanes of
-      // its sub-partition, whichever warpgroup accumulated them).  The
-      // exchange overwrites the query tile, so each warpgroup first sees
+      // warpgroup w finishes columns [w D/2, (w + 1) D/2) of every row,
+      // reading them from both O accumulators (any warp may read the TMEM
+      // lanes of its sub-partition, whichever warpgroup accumulated them).
+      // The exchange overwrites the query tile, so each warpgroup first sees
       // both warpgroups' last products complete: their commits follow the
       // issue of every Q K^T (a warpgroup without a key tile has not waited
       // for any yet).
@@ -762,68 +762,68 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ok = __all_sync(0xffffffffu, mbar_wait(&o_done[1], (nkv1 - 1) & 1, wc, ATTN_ETIMEOUT));
       if (wg == 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&o_done[0], (nkv0 - 1) & 1, wc, ATTN_ETIMEOUT));
-    }
-    if (single && ok) {
-      x_m[wg * kBlockM + row] = m_ref;
-      x_d[wg * kBlockM + row] = dsum;
-      mbar_arrive(xchg);
-      ok = __all_sync(0xffffffffu, mbar_wait(xchg, 0, wc, ATTN_ETIMEOUT));
       if (ok) {
-        tc_fence_after();
-        const float m0 = x_m[row], m1 = x_m[kBlockM + row];
-        const float m = fmaxf(m0, m1);  // m0 is finite: warpgroup 0 always has a key tile
-        const float a0 = ex2_approx(m0 - m);
-        const float a1 = nkv1 > 0 ? ex2_approx(m1 - m) : 0.f;
-        const float d = a0 * x_d[row] + a1 * x_d[kBlockM + row];
-        const float inv = o_scale / d;  // o_scale: the E4M3 kernel's V descale, else 1
-        const float2 c0 = make_float2(a0 * inv, a0 * inv), c1 = make_float2(a1 * inv, a1 * inv);
-        const uint32_t tO0 = tmem + kOCol + lane_off, tO1 = tmem + kOCol + kOStride + lane_off;
-        // O as fp16 into the first K/V stages (free: every product has
-        // completed), in the 128B-swizzled layout of the 64-column TMA box:
-        // at D = 128 warpgroup w fills box w, at D = 64 the two warpgroups
-        // fill the halves of one box.  Rows past Nq are not stored.
-        uint8_t* so = sK;
+        x_m[wg * kBlockM + row] = m_ref;
+        x_d[wg * kBlockM + row] = dsum;
+        mbar_arrive(xchg);
+        ok = __all_sync(0xffffffffu, mbar_wait(xchg, 0, wc, ATTN_ETIMEOUT));
+        if (ok) {
+          tc_fence_after();
+          const float m0 = x_m[row], m1 = x_m[kBlockM + row];
+          const float m = fmaxf(m0, m1);  // m0 is finite: warpgroup 0 always has a key tile
+          const float a0 = ex2_approx(m0 - m);
+          const float a1 = nkv1 > 0 ? ex2_approx(m1 - m) : 0.f;
+          const float d = a0 * x_d[row] + a1 * x_d[kBlockM + row];
+          const float inv = o_scale / d;  // o_scale: the E4M3 kernel's V descale, else 1
+          const float2 c0 = make_float2(a0 * inv, a0 * inv), c1 = make_float2(a1 * inv, a1 * inv);
+          const uint32_t tO0 = tmem + kOCol + lane_off, tO1 = tmem + kOCol + kOStride + lane_off;
+          // O as fp16 into the first K/V stages (free: every product has
+          // completed), in the 128B-swizzled layout of the 64-column TMA box:
+          // at D = 128 warpgroup w fills box w, at D = 64 the two warpgroups
+          // fill the halves of one box.  Rows past Nq are not stored.
+          uint8_t* so = sK;
 #pragma unroll
-        for (int cc = 0; cc < HD / 64; ++cc) {
-          const int c = wg * (HD / 64) + cc;  // this warpgroup's 32-column chunks
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tO0 + c * 32, o0);
-          if (nkv1 > 0) tmem_ld32(tO1 + c * 32, o1);
-          tmem_ld_wait(o0);
-          if (nkv1 > 0) {
-            tmem_ld_wait(o1);
-          } else {
+          for (int cc = 0; cc < HD / 64; ++cc) {
+            const int c = wg * (HD / 64) + cc;  // this warpgroup's 32-column chunks
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tO0 + c * 32, o0);
+            if (nkv1 > 0) tmem_ld32(tO1 + c * 32, o1);
+            tmem_ld_wait(o0);
+            if (nkv1 > 0) {
+              tmem_ld_wait(o1);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o1[e] = 0u;
+              for (int e = 0; e < 32; ++e) o1[e] = 0u;
+            }
+            uint32_t h[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 v = __ffma2_rn(make_float2(__uint_as_float(o1[2 * e]), __uint_as_float(o1[2 * e + 1])), c1,
+                                          __fmul2_rn(make_float2(__uint_as_float(o0[2 * e]), __uint_as_float(o0[2 * e + 1])), c0));
+              h[e] = pack_half2(v.x, v.y);
+            }
+            uint8_t* srow = so + (c >> 1) * kChunkBytes + row * 128;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int u = (c & 1) * 4 + e;
+              *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) =
+                  make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
+            }
           }
-          uint32_t h[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 v = __ffma2_rn(make_float2(__uint_as_float(o1[2 * e]), __uint_as_float(o1[2 * e + 1])), c1,
-                                        __fmul2_rn(make_float2(__uint_as_float(o0[2 * e]), __uint_as_float(o0[2 * e + 1])), c0));
-            h[e] = pack_half2(v.x, v.y);
+          fence_proxy_async_smem();
+          mbar_arrive(&o_staged[wg]);
+          if (row == 0 && (HD == 128 || wg == 0)) {
+            bool staged = mbar_wait(&o_staged[wg], 0, wc, ATTN_ETIMEOUT);
+            if (HD == 64 && staged) staged = mbar_wait(&o_staged[1], 0, wc, ATTN_ETIMEOUT);
+            if (staged) {
+              tma_store_3d(&tmO, so + wg * kChunkBytes, 64 * wg, rw, bh);
+              bulk_commit_group();
+              bulk_wait_read_all();
+            }
           }
-          uint8_t* srow = so + (c >> 1) * kChunkBytes + row * 128;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int u = (c & 1) * 4 + e;
-            *reinterpret_cast<uint4*>(srow + ((u ^ (row & 7)) << 4)) =
-                make_uint4(h[4 * e], h[4 * e + 1], h[4 * e + 2], h[4 * e + 3]);
-          }
+          if (wg == 0 && lse != nullptr && i < Nq)
+            lse[static_cast<size_t>(bh) * Nq + i] = (m + log2f(d)) * 0.69314718055994531f;
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&o_staged[wg]);
-        if (row == 0 && (HD == 128 || wg == 0)) {
-          bool staged = mbar_wait(&o_staged[wg], 0, wc, ATTN_ETIMEOUT);
-          if (HD == 64 && staged) staged = mbar_wait(&o_staged[1], 0, wc, ATTN_ETIMEOUT);
-          if (staged) {
-            tma_store_3d(&tmO, so + wg * kChunkBytes, 64 * wg, rw, bh);
-            bulk_commit_group();
-            bulk_wait_read_all();
-          }
-        }
-        if (wg == 0 && lse != nullptr && i < Nq)
-          lse[static_cast<size_t>(bh) * Nq + i] = (m + log2f(d)) * 0.69314718055994531f;
       }
     } else if (ok && my_nkv > 0 && !SPLITKV) {
       // ---------------------------------------------------------- epilogue

@@ -81,12 +81,12 @@ def gpu_local_cpus(dev_index: int):
 
 
 def _strip_comments(src: str) -> str:
-    """C/C++ source without comments and blank-only lines (string literals in
-    these files hold no comment markers)."""
+    """C/C++ source without comments, blank lines and the indentation of each
+    line (string literals in these files hold no comment markers)."""
     import re
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
-    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+    return "\n".join(line.strip() for line in src.splitlines() if line.strip())
 
 
 def kernel_source_digest() -> str:
