@@ -286,9 +286,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     pair = item % n_pairs;
     bh = item / n_pairs;
   } else {
-    bh = static_cast<int>(blockIdx.y);
-    pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-    if (static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x) >= n_main) return;  // left to the single-tile launch
+    const int lin = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);  // the order CTAs are dispatched in
+    if constexpr (CAUSAL) {
+      // Causal pairs cost in proportion to their index (pair p visits 2p + 2
+      // key tiles).  Heaviest first across all heads: the first CTAs take
+      // every head's last pair, then every head's pair before it, and so
+      // on, so the light pairs fill the end of the grid (a longest-first
+      // list schedule on the SMs as they free up).
+      const int nbh = static_cast<int>(gridDim.y);
+      pair = static_cast<int>(gridDim.x) - 1 - lin / nbh;
+      bh = lin % nbh;
+    } else {
+      bh = static_cast<int>(blockIdx.y);
+      pair = static_cast<int>(blockIdx.x);
+      if (lin >= n_main) return;  // left to the single-tile launch
+    }
   }
   const int r0 = pair * kRowsPerCta;
   // Key tiles of this CTA: all of the pair's (grid z = 1), or with split-KV
