@@ -461,16 +461,21 @@ def main():
         for _ in range(2):
             e2e_step()
         barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n_e2e):
+        # one event per step boundary on the caller's stream (each call's
+        # copies and forward start after the previous call's last copy out)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+        marks[0].record(stream)
+        for s in range(n_e2e):
             e2e_step()
-        b.record(stream)
+            marks[s + 1].record(stream)
         barrier()
-        e_ms = a.elapsed_time(b) / n_e2e
+        step_e2e = [marks[s].elapsed_time(marks[s + 1]) for s in range(n_e2e)]
+        e_ms = marks[0].elapsed_time(marks[n_e2e]) / n_e2e
         e_ms = multirank.max_over_ranks(e_ms, dist, dev)
         e2e = {"value": multirank.aggregate_tflops(f, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "steps": n_e2e,
+               "step_ms": {"median": statistics.median(step_e2e), "p10": percentile(step_e2e, 10),
+                           "p90": percentile(step_e2e, 90), "max": max(step_e2e)},
                "h2d_gbs_measured": h2d_gbs,
                "d2h_gbs_measured": d2h_gbs,
                "host_buffers": (f"pinned, first touched on the {len(local_cpus)} CPUs local to the GPU"
