@@ -207,14 +207,28 @@ def test_argument_errors_on_device():
 
 # ------------------------------------------------------------ maximum sizes
 
-def test_max_heads_grid_limit():
+@pytest.mark.parametrize("causal", [False, True])
+def test_max_heads_grid_limit(causal):
     """B*H = 65535, the largest head count the grid takes: every (b, h) is its
-    own problem; compared in full (one query row, three keys each)."""
-    B, H, Nq, Nk, D = 3, 21845, 1, 3, 64
+    own problem; compared in full (three query rows, three keys each)."""
+    B, H, Nq, Nk, D = 3, 21845, 3, 3, 64
     q, k, v = synth.make_qkv(B, H, Nq, Nk, D, seed=41)
-    o, lse = run_gpu(q, k, v, 0.125, False)
-    O, L = oracle.attn_full(q, k, v, 0.125, False)
-    compare(o, lse, O, L, "B*H = 65535")
+    o, lse = run_gpu(q, k, v, 0.125, causal)
+    O, L = oracle.attn_full(q, k, v, 0.125, causal)
+    compare(o, lse, O, L, f"B*H = 65535, causal={causal}")
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,D", [
+    (2, 3, 700, 700, 128),   # 6 heads x 3 pairs, the last pair ragged
+    (2, 3, 700, 700, 64),
+    (1, 7, 1300, 900, 128),  # Nq > Nk: the last query tiles see every key
+    (3, 5, 520, 1100, 64),   # Nq < Nk
+])
+def test_causal_pairs_heaviest_first_across_heads(B, H, Nq, Nk, D):
+    """Causal CTAs take the pairs of all heads in decreasing pair order (the
+    linear CTA index mapped pair-major): every (head, pair) must be computed
+    exactly once, ragged pairs included; compared in full."""
+    full_parity(B, H, Nq, Nk, D, True, seed=700 + B * H + Nq + D)
 
 
 @pytest.mark.parametrize("Nk,D", [(1 << 16, 64), (1 << 18, 64), (1 << 19, 64), (1 << 19, 128)])
