@@ -54,11 +54,12 @@
 //     tiles up to its own diagonal; only the diagonal and the ragged last
 //     tile take the masked path.
 //
-//   * Wave quantisation (non-causal single pass, fp16 and E4M3): when a
-//     launch's last wave of CTAs would occupy at most half the SMs, its
-//     pairs run as a second launch of CTAs that each take one query tile,
-//     the two warpgroups alternating its key tiles and merging their
-//     carriers at the end -- twice the CTAs, half the work each.
+//   * Wave quantisation (single pass, fp16 and E4M3): when a launch's last
+//     wave of CTAs would occupy at most half the SMs, its pairs run as a
+//     second launch of CTAs that each take one query tile, the two
+//     warpgroups alternating its key tiles and merging their carriers at
+//     the end -- twice the CTAs, half the work each.  Causal: only grids
+//     below half a wave, which run as single-tile CTAs alone.
 //
 // TMEM (512 columns): at D = 128, S_0/P_0 [0,128), S_1/P_1 [128,256),
 // O_0 [256,384), O_1 [384,512).  At D = 64 three score slots [0,128),
@@ -267,7 +268,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int lane = threadIdx.x & 31;
   // Work of this CTA.  Usually two query tiles of one (batch, head) -- a
   // pair -- each warpgroup taking one of them against every key tile (of the
-  // share, with split-KV).  SINGLE (the non-causal single pass):
+  // share, with split-KV).  SINGLE (the single pass):
   // one query tile, both warpgroups sharing its key range -- warpgroup w
   // takes key tiles w, w + 2, ... -- and merging their two partial results
   // at the end.  The host runs the pairs of a last partial wave that would
@@ -276,7 +277,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // (n_main: the pairs it keeps, in (head, pair) order), and the single-
   // tile launch's CTA b takes query tile b % 2 of pair n_main + b / 2.
   constexpr bool single = SINGLE;
-  static_assert(!SINGLE || (SLOTS == 2 && !SPLITKV && !CAUSAL), "single-tile CTAs");
+  static_assert(!SINGLE || (SLOTS == 2 && !SPLITKV), "single-tile CTAs");
   int bh, pair, half = 0;
   if constexpr (SINGLE) {
     const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
@@ -1303,17 +1304,22 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 }
 
 // One forward: the grid of (query-tile pair, head, share) CTAs.  For the
-// non-causal single pass (fp16 or E4M3), the pairs of a last partial wave that
-// would occupy at most half the SMs go to a second launch of single-tile
-// CTAs (two per pair, half the work each), which runs as soon as the full
-// waves are done: that wave then takes half as long.
+// single pass (fp16 or E4M3), the pairs of a last partial wave that would
+// occupy at most half the SMs go to a second launch of single-tile CTAs
+// (two per pair, half the work each), which runs as soon as the full waves
+// are done: that wave then takes half as long (causal: grids below half a
+// wave only, as one launch of single-tile CTAs).
 // Pairs of the last partial wave that go to single-tile CTAs: all of the
 // last wave's pairs when it would occupy at most half of the `sms` SMs --
 // and, when full waves of pairs come first, only if each query tile has at
 // least 16 key tiles: the second launch then waits for the full waves and
 // costs a few microseconds, more than half a wave of short CTAs saves.
-int64_t tail_pairs(int64_t pairs, int sms, int key_tiles) {
+// Causal: only a whole grid below half a wave.  Its pairs are ordered
+// heaviest first, so a last partial wave holds the lightest pairs, and a
+// second launch would wait for the heaviest.
+int64_t tail_pairs(int64_t pairs, int sms, int key_tiles, bool causal) {
   if (sms <= 0) return 0;
+  if (causal) return 2 * pairs <= sms ? pairs : 0;
   const int64_t last = pairs % sms;
   if (last == 0 || 2 * last > sms) return 0;
   if (last < pairs && key_tiles < 16) return 0;
@@ -1327,8 +1333,8 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
                const RunCtl& rc, float o_scale = 1.0f) {
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
-  constexpr bool kTail = !SPLITKV && !CAUSAL;
-  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms, (Nk + kBlockN - 1) / kBlockN) : 0;
+  constexpr bool kTail = !SPLITKV;
+  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms, (Nk + kBlockN - 1) / kBlockN, CAUSAL) : 0;
   if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
   const int n_main = static_cast<int>(pairs - tail);
   if (n_main > 0) {
@@ -1627,9 +1633,8 @@ int attn_fwd_launch_count(int B, int H, int Nq, int Nk, int D, int causal) {
     if (r != ATTN_OK) return -r;
     sms = st->sms;
   }
-  if (causal) return 1;
   const int64_t pairs = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
-  const int64_t tail = tail_pairs(pairs, sms, (Nk + kBlockN - 1) / kBlockN);
+  const int64_t tail = tail_pairs(pairs, sms, (Nk + kBlockN - 1) / kBlockN, causal != 0);
   return (pairs - tail > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);
 }
 

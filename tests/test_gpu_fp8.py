@@ -114,6 +114,17 @@ def test_fp8_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk, heads):
     check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, False, vd=0.5, rows=rows, label=f"[{B},{H},{Nq},{Nk}] partial wave")
 
 
+def test_fp8_causal_pairs_above_half_a_wave():
+    """Causal E4M3 with 160 pairs, so the pair kernel runs (the small causal
+    cases above run as single-query-tile CTAs); every row of a few heads."""
+    B, H, Nq, Nk = 2, 40, 512, 512
+    q8, k8, v8 = synth.make_qkv_e4m3(B, H, Nq, Nk, 128, seed=4400, sigma_qk=2.0)
+    o, lse = run_fp8(q8, k8, v8, 128 ** -0.5, True)
+    heads = (0, 1, 39, 40, 78, 79)
+    rows = np.concatenate([np.arange(bh * Nq, (bh + 1) * Nq) for bh in heads])
+    check_fp8(o, lse, q8, k8, v8, 128 ** -0.5, True, rows=rows, label="causal E4M3 pairs")
+
+
 def test_fp8_descales():
     q8, k8, v8 = synth.make_qkv_e4m3(1, 2, 256, 2048, 128, seed=4100, sigma_qk=2.0)
     args = dict(qd=0.5, kd=3.0, vd=0.25)

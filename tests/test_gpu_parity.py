@@ -219,16 +219,31 @@ def test_max_heads_grid_limit(causal):
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,D", [
-    (2, 3, 700, 700, 128),   # 6 heads x 3 pairs, the last pair ragged
-    (2, 3, 700, 700, 64),
-    (1, 7, 1300, 900, 128),  # Nq > Nk: the last query tiles see every key
-    (3, 5, 520, 1100, 64),   # Nq < Nk
+    (2, 40, 700, 700, 128),   # 80 heads x 3 pairs, the last pair ragged
+    (2, 40, 700, 700, 64),
+    (1, 80, 1300, 900, 128),  # Nq > Nk: the last query tiles see every key
+    (3, 30, 520, 1100, 64),   # Nq < Nk
 ])
 def test_causal_pairs_heaviest_first_across_heads(B, H, Nq, Nk, D):
     """Causal CTAs take the pairs of all heads in decreasing pair order (the
     linear CTA index mapped pair-major): every (head, pair) must be computed
-    exactly once, ragged pairs included; compared in full."""
+    exactly once, ragged pairs included; compared in full.  (More than half
+    a wave of pairs, so these run as pair CTAs.)"""
     full_parity(B, H, Nq, Nk, D, True, seed=700 + B * H + Nq + D)
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,D", [
+    (1, 2, 1000, 1000, 128),  # 8 pairs: 16 single-tile CTAs, the last tile ragged
+    (1, 4, 2048, 2048, 64),
+    (2, 3, 700, 900, 128),    # Nq < Nk
+    (1, 1, 4096, 4096, 128),  # one head, 32 query tiles of 1..32 key tiles
+    (1, 3, 900, 300, 64),     # Nq > Nk
+])
+def test_causal_small_grids_as_single_query_tiles(B, H, Nq, Nk, D):
+    """Causal grids below half a wave run as single-query-tile CTAs (the two
+    warpgroups alternate the tile's key tiles, the diagonal one masked in
+    whichever takes it, and merge their carriers); compared in full."""
+    full_parity(B, H, Nq, Nk, D, True, seed=900 + B * H + Nq + Nk + D)
 
 
 @pytest.mark.parametrize("Nk,D", [(1 << 16, 64), (1 << 18, 64), (1 << 19, 64), (1 << 19, 128)])
@@ -304,14 +319,15 @@ def test_huge_jump_of_the_running_max(causal):
 def test_launch_count_reports_the_single_tile_launch():
     """attn_fwd_launch_count: two kernels exactly when the non-causal
     forward re-runs a last partial wave of at most half the SMs as
-    single-query-tile CTAs next to full waves of pairs; one otherwise."""
+    single-query-tile CTAs next to full waves of pairs; one otherwise
+    (causal grids below half a wave are one launch of single-tile CTAs)."""
     torch = torch_cuda()
     import attention_forward_12_gb300 as attn
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
     def expected(B, H, Nq, Nk, D, causal):
         pairs = B * H * ((Nq + 255) // 256)
-        if causal:
+        if causal:  # pairs, or single-tile CTAs alone below half a wave: one launch either way
             return 1
         last = pairs % sms
         tail = last if (last > 0 and 2 * last <= sms) else 0
@@ -322,7 +338,8 @@ def test_launch_count_reports_the_single_tile_launch():
     for (B, H, Nq, Nk, D, causal) in [(1, 16, 8192, 8192, 128, False), (4, 32, 16384, 16384, 128, False),
                                       (1, 4, 512, 8192, 128, False), (2, 16, 16384, 16384, 128, True),
                                       (1, 8, 4096, 4096, 64, False), (1, 80, 300, 300, 128, False),
-                                      (1, 80, 300, 4096, 128, False), (2, 40, 512, 512, 64, False)]:
+                                      (1, 80, 300, 4096, 128, False), (2, 40, 512, 512, 64, False),
+                                      (1, 2, 1000, 1000, 128, True)]:
         assert attn.fwd_launch_count(B, H, Nq, Nk, D, causal) == expected(B, H, Nq, Nk, D, causal)
     assert attn.fwd_launch_count(0, 4, 128, 128, 128, False) == 0
     assert attn.fwd_launch_count(1, 4, 128, 128, 96, False) == -attn.ATTN_EINVAL
