@@ -59,7 +59,7 @@
 //     second launch of CTAs that each take one query tile, the two
 //     warpgroups alternating its key tiles and merging their carriers at
 //     the end -- twice the CTAs, half the work each.  Causal: only grids
-//     below half a wave, which run as single-tile CTAs alone.
+//     of at most one wave of pairs, which run as single-tile CTAs alone.
 //
 // TMEM (512 columns): at D = 128, S_0/P_0 [0,128), S_1/P_1 [128,256),
 // O_0 [256,384), O_1 [384,512).  At D = 64 three score slots [0,128),
@@ -282,10 +282,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if constexpr (SINGLE) {
     const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
     const int b = static_cast<int>(blockIdx.x);
-    const int item = n_main + (b >> 1);
-    half = b & 1;
-    pair = item % n_pairs;
-    bh = item / n_pairs;
+    if constexpr (CAUSAL) {
+      // The whole grid (n_main = 0), heaviest query tile first across all
+      // heads, as for the causal pairs: a query tile t visits t + 1 key tiles.
+      const int nbh = static_cast<int>(gridDim.x) / (2 * n_pairs);
+      const int qt = 2 * n_pairs - 1 - b / nbh;
+      bh = b % nbh;
+      pair = qt >> 1;
+      half = qt & 1;
+    } else {
+      const int item = n_main + (b >> 1);
+      half = b & 1;
+      pair = item % n_pairs;
+      bh = item / n_pairs;
+    }
   } else {
     const int lin = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);  // the order CTAs are dispatched in
     if constexpr (CAUSAL) {
@@ -1307,19 +1317,20 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 // single pass (fp16 or E4M3), the pairs of a last partial wave that would
 // occupy at most half the SMs go to a second launch of single-tile CTAs
 // (two per pair, half the work each), which runs as soon as the full waves
-// are done: that wave then takes half as long (causal: grids below half a
-// wave only, as one launch of single-tile CTAs).
+// are done: that wave then takes half as long (causal: grids of at most one
+// wave of pairs only, as one launch of single-tile CTAs).
 // Pairs of the last partial wave that go to single-tile CTAs: all of the
 // last wave's pairs when it would occupy at most half of the `sms` SMs --
 // and, when full waves of pairs come first, only if each query tile has at
 // least 16 key tiles: the second launch then waits for the full waves and
 // costs a few microseconds, more than half a wave of short CTAs saves.
-// Causal: only a whole grid below half a wave.  Its pairs are ordered
-// heaviest first, so a last partial wave holds the lightest pairs, and a
-// second launch would wait for the heaviest.
+// Causal: only a whole grid of at most one wave of pairs, which then runs
+// as single-tile CTAs alone, heaviest first (up to two waves of them: the
+// light tiles of the triangle fill the second).  Larger causal grids keep
+// their pairs, ordered heaviest first, whose last wave holds the lightest.
 int64_t tail_pairs(int64_t pairs, int sms, int key_tiles, bool causal) {
   if (sms <= 0) return 0;
-  if (causal) return 2 * pairs <= sms ? pairs : 0;
+  if (causal) return pairs <= sms ? pairs : 0;
   const int64_t last = pairs % sms;
   if (last == 0 || 2 * last > sms) return 0;
   if (last < pairs && key_tiles < 16) return 0;

@@ -238,11 +238,14 @@ def test_causal_pairs_heaviest_first_across_heads(B, H, Nq, Nk, D):
     (2, 3, 700, 900, 128),    # Nq < Nk
     (1, 1, 4096, 4096, 128),  # one head, 32 query tiles of 1..32 key tiles
     (1, 3, 900, 300, 64),     # Nq > Nk
+    (1, 8, 4096, 4096, 64),   # 128 pairs: 256 single-tile CTAs, heaviest first over two waves
+    (2, 4, 3000, 3000, 128),  # 96 pairs, the last query tile of each head ragged
 ])
 def test_causal_small_grids_as_single_query_tiles(B, H, Nq, Nk, D):
-    """Causal grids below half a wave run as single-query-tile CTAs (the two
-    warpgroups alternate the tile's key tiles, the diagonal one masked in
-    whichever takes it, and merge their carriers); compared in full."""
+    """Causal grids of at most one wave of pairs run as single-query-tile
+    CTAs, heaviest first across heads (the two warpgroups alternate the
+    tile's key tiles, the diagonal one masked in whichever takes it, and
+    merge their carriers); compared in full."""
     full_parity(B, H, Nq, Nk, D, True, seed=900 + B * H + Nq + Nk + D)
 
 
