@@ -1328,13 +1328,22 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
 // as single-tile CTAs alone, heaviest first (up to two waves of them: the
 // light tiles of the triangle fill the second).  Larger causal grids keep
 // their pairs, ordered heaviest first, whose last wave holds the lightest.
-int64_t tail_pairs(int64_t pairs, int sms, int key_tiles, bool causal) {
+// Non-causal grids whose pairs are often half empty (a query length that
+// leaves the second tile of a head's last pair past Nq) also run as
+// single-tile CTAs alone when that takes clearly fewer waves: a single-tile
+// CTA costs about 0.65 of a pair CTA over the same key tiles (measured
+// 0.57-0.6 on long key ranges), and only the query tiles that exist cost
+// anything.  `q_tiles` counts those over all heads.
+int64_t tail_pairs(int64_t pairs, int sms, int key_tiles, bool causal, int64_t q_tiles) {
   if (sms <= 0) return 0;
   if (causal) return pairs <= sms ? pairs : 0;
   const int64_t last = pairs % sms;
-  if (last == 0 || 2 * last > sms) return 0;
-  if (last < pairs && key_tiles < 16) return 0;
-  return last;
+  int64_t tail = last;
+  if (last == 0 || 2 * last > sms || (last < pairs && key_tiles < 16)) tail = 0;
+  const double waves_now = static_cast<double>((pairs - tail + sms - 1) / sms) + (tail > 0 ? 0.65 : 0.0);
+  const double waves_single = 0.65 * static_cast<double>((q_tiles + sms - 1) / sms);
+  if (waves_single < 0.9 * waves_now) return pairs;
+  return tail;
 }
 
 template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool FP8 = false, int SLOTS = 2>
@@ -1345,7 +1354,8 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   const int n_pairs = (Nq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t pairs = static_cast<int64_t>(n_pairs) * BH;
   constexpr bool kTail = !SPLITKV;
-  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms, (Nk + kBlockN - 1) / kBlockN, CAUSAL) : 0;
+  const int64_t q_tiles = static_cast<int64_t>(BH) * ((Nq + kBlockM - 1) / kBlockM);
+  const int64_t tail = kTail ? tail_pairs(pairs, rc.sms, (Nk + kBlockN - 1) / kBlockN, CAUSAL, q_tiles) : 0;
   if (pairs > 0x7fffffff) return ATTN_EUNSUPPORTED;
   const int n_main = static_cast<int>(pairs - tail);
   if (n_main > 0) {
@@ -1645,7 +1655,8 @@ int attn_fwd_launch_count(int B, int H, int Nq, int Nk, int D, int causal) {
     sms = st->sms;
   }
   const int64_t pairs = static_cast<int64_t>(B) * H * ((Nq + kRowsPerCta - 1) / kRowsPerCta);
-  const int64_t tail = tail_pairs(pairs, sms, (Nk + kBlockN - 1) / kBlockN, causal != 0);
+  const int64_t q_tiles = static_cast<int64_t>(B) * H * ((Nq + kBlockM - 1) / kBlockM);
+  const int64_t tail = tail_pairs(pairs, sms, (Nk + kBlockN - 1) / kBlockN, causal != 0, q_tiles);
   return (pairs - tail > 0 ? 1 : 0) + (tail > 0 ? 1 : 0);
 }
 

@@ -107,7 +107,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * last partial wave that would occupy at most half the SMs run as a second
  * launch of single-query-tile CTAs after full waves of pairs (done when a
  * query tile has 16 key tiles or more; a grid of less than half a wave,
- * or a causal grid of at most one wave, runs as single-query-tile CTAs
+ * a causal grid of at most one wave, or a grid of half-empty pairs that
+ * takes clearly fewer waves that way, runs as single-query-tile CTAs
  * alone, in one launch).  0
  * when there is nothing to compute.  For counting launches, e.g. in a
  * benchmark.  Returns

@@ -97,7 +97,7 @@ def test_fp8_matches_oracle(B, H, Nq, Nk, causal, sqk, seed):
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,heads", [
-    # 160 pairs: on 152 SMs the last 8 (heads 76-79) run as single query tiles
+    # 160 half-empty pairs: all 240 query tiles as single-tile CTAs
     (1, 80, 300, 2100, (0, 1, 37, 75, 76, 77, 78, 79)),
     # 160 pairs with 17 key tiles each: warpgroup 0 of a single-tile CTA holds the ragged one
     (2, 40, 512, 2049, (0, 38, 39, 76, 77, 78, 79)),

@@ -60,10 +60,11 @@ def test_edge_shapes(B, H, Nq, Nk, D, causal):
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,D", [
-    (1, 80, 300, 2100, 128),  # 160 pairs: on 152 SMs the last 8 run as single query tiles, some past Nq
+    (1, 80, 300, 2100, 128),  # 160 half-empty pairs: all 240 query tiles as single-tile CTAs
     (1, 3, 1000, 777, 128),   # 12 pairs, all as single query tiles (an odd key tile count per tile)
     (2, 40, 512, 2049, 128),  # 160 pairs, 17 key tiles each: warpgroup 0 holds the ragged one
     (1, 80, 300, 2100, 64),   # the same at D=64 (single-tile CTAs with two score slots)
+    (1, 40, 300, 2100, 128),  # 80 half-empty pairs, below a wave: single-tile CTAs
     (1, 3, 1000, 777, 64),
 ])
 def test_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk, D):
@@ -71,7 +72,8 @@ def test_partial_last_wave_as_single_query_tiles(B, H, Nq, Nk, D):
     SMs are re-run as CTAs of one query tile, both warpgroups sharing its key
     tiles and merging their carriers (every other shape of these tests with
     few heads takes that path too).  After full waves of pairs this needs 16
-    key tiles or more per query tile."""
+    key tiles or more per query tile.  Grids of half-empty pairs run as
+    single-tile CTAs alone when that takes clearly fewer waves."""
     full_parity(B, H, Nq, Nk, D, False, seed=500 + H + Nk + D)
 
 
@@ -330,19 +332,25 @@ def test_launch_count_reports_the_single_tile_launch():
 
     def expected(B, H, Nq, Nk, D, causal):
         pairs = B * H * ((Nq + 255) // 256)
-        if causal:  # pairs, or single-tile CTAs alone below half a wave: one launch either way
+        if causal:  # pairs, or single-tile CTAs alone up to one wave: one launch either way
             return 1
         last = pairs % sms
         tail = last if (last > 0 and 2 * last <= sms) else 0
         if 0 < tail < pairs and (Nk + 127) // 128 < 16:  # short CTAs: no second launch after full waves
             tail = 0
+        # all single-tile CTAs when the existing query tiles take clearly fewer waves that way
+        q_tiles = B * H * ((Nq + 127) // 128)
+        waves_now = -(-(pairs - tail) // sms) + (0.65 if tail else 0.0)
+        if 0.65 * -(-q_tiles // sms) < 0.9 * waves_now:
+            tail = pairs
         return int(pairs - tail > 0) + int(tail > 0)
 
     for (B, H, Nq, Nk, D, causal) in [(1, 16, 8192, 8192, 128, False), (4, 32, 16384, 16384, 128, False),
                                       (1, 4, 512, 8192, 128, False), (2, 16, 16384, 16384, 128, True),
                                       (1, 8, 4096, 4096, 64, False), (1, 80, 300, 300, 128, False),
                                       (1, 80, 300, 4096, 128, False), (2, 40, 512, 512, 64, False),
-                                      (1, 2, 1000, 1000, 128, True)]:
+                                      (1, 2, 1000, 1000, 128, True), (1, 40, 300, 2100, 128, False),
+                                      (2, 40, 512, 2049, 128, False)]:
         assert attn.fwd_launch_count(B, H, Nq, Nk, D, causal) == expected(B, H, Nq, Nk, D, causal)
     assert attn.fwd_launch_count(0, 4, 128, 128, 128, False) == 0
     assert attn.fwd_launch_count(1, 4, 128, 128, 96, False) == -attn.ATTN_EINVAL
