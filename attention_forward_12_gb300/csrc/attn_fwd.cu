@@ -312,6 +312,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       pair = static_cast<int>(blockIdx.x);
       if (lin >= n_main) return;  // left to the single-tile launch
     }
+    // A single-tile launch that follows may start once every CTA here has
+    // started (no-op without one).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
   const int r0 = pair * kRowsPerCta;
   // Key tiles of this CTA: all of the pair's (grid z = 1), or with split-KV
@@ -967,6 +970,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // A single-tile launch that may have started next to the pairs' launch
+  // (see launch_kernel) ends only after that grid has completed, so the
+  // forward as a whole completes in stream order (no-op otherwise).
+  if constexpr (SINGLE) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Merge of the split-KV parts: the carrier merge of partial states
@@ -1281,7 +1288,7 @@ template <int HD, bool CAUSAL, int NS, int SPLIT_P, int EMU, bool SPLITKV, bool 
 int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
                   void* o, float* lse,
                   float* ws_o, float* ws_l, dim3 grid, int Nq, int Nk, float sl2, int n_main, cudaStream_t st,
-                  const RunCtl& rc, float o_scale) {
+                  const RunCtl& rc, float o_scale, bool after_pairs = false) {
   using L = Layout<HD, NS, FP8, SINGLE ? 1 : 2>;
   auto kern = attn_fwd_kernel<HD, CAUSAL, NS, SPLIT_P, EMU, SPLITKV, FP8, SLOTS, SINGLE>;
   static_assert(L::kSmem <= 232448, "shared memory budget");
@@ -1298,9 +1305,33 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
       return ATTN_ECUDA;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, mo, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
-  if (cudaGetLastError() == cudaSuccess) return ATTN_OK;
+  // The single-tile launch that follows a launch of pairs may start while
+  // the pairs' last wave still runs (programmatic dependent launch): its
+  // CTAs take SMs as they free up instead of after the slowest pair CTA
+  // and a launch gap.  The two grids touch disjoint rows, and each
+  // single-tile CTA waits for the pairs' grid before it exits, so work
+  // after the forward on the stream still follows all of it.
+  auto launch = [&]() -> cudaError_t {
+    if (!after_pairs) {
+      kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, mo, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
+                                             o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
+      return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
+                              o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
+  };
+  if (launch() == cudaSuccess) return ATTN_OK;
+  cudaGetLastError();
   // A context reset (cudaDeviceReset) drops the attribute: set it again and
   // retry once (a launch that failed did not run).
   attr_set.fetch_and(~bit, std::memory_order_acq_rel);
@@ -1308,9 +1339,7 @@ int launch_kernel(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
       cudaSuccess)
     return ATTN_ECUDA;
   attr_set.fetch_or(bit, std::memory_order_release);
-  kern<<<grid, kThreads, L::kSmem, st>>>(mq, mk, mv, mo, static_cast<__half*>(o), lse, ws_o, ws_l, Nq, Nk, sl2,
-                                         o_scale, rc.status_dev, rc.timeout_ns, rc.drop, n_main);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
+  return launch() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
 // One forward: the grid of (query-tile pair, head, share) CTAs.  For the
@@ -1369,7 +1398,7 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     if (tail > 0)
       return launch_kernel<HD, CAUSAL, single_stages<HD, FP8>(), SPLIT_P, EMU, SPLITKV, FP8, 2, true>(
           mq, mk, mv, mo, o, lse, ws_o, ws_l, dim3(static_cast<unsigned>(2 * tail)), Nq, Nk, sl2, n_main, st, rc,
-          o_scale);
+          o_scale, n_main > 0);
   }
   return ATTN_OK;
 }
