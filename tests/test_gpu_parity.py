@@ -188,6 +188,32 @@ def test_side_stream():
     compare(o.cpu().numpy(), lse.cpu().numpy(), O, L, "side stream")
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk,D", [(2, 40, 512, 2049, 128), (1, 16, 8192, 8192, 64)])
+def test_stream_order_after_the_dependent_launch(B, H, Nq, Nk, D):
+    """A launch of pairs followed by a dependent single-tile launch: work
+    queued after the forward on the same stream, with no synchronisation in
+    between, must see all of O (the single-tile CTAs wait for the pairs'
+    grid before they exit).  Copies taken at once, several times, must equal
+    the output read after a synchronisation."""
+    torch = torch_cuda()
+    import attention_forward_12_gb300 as attn
+    assert attn.fwd_launch_count(B, H, Nq, Nk, D, False) == 2
+    qn, kn, vn = synth.make_qkv(B, H, Nq, Nk, D, seed=77)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (qn, kn, vn))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    copies = []
+    for _ in range(4):
+        o.fill_(float("nan"))
+        attn.fwd(q, k, v, causal=False, out=o, lse=lse)
+        copies.append((o.clone(), lse.clone()))  # same stream, no synchronisation
+    torch.cuda.synchronize()
+    assert attn.get_status() == attn.ATTN_OK
+    for oc, lc in copies:
+        assert torch.equal(oc, o) and torch.equal(lc, lse)
+    assert not torch.isnan(o).any()
+
+
 def test_argument_errors_on_device():
     torch = torch_cuda()
     import attention_forward_12_gb300 as attn
