@@ -12,12 +12,14 @@ from gpu_common import torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("D,causal", [(64, False), (128, True)])
-def test_forward_replays_from_a_cuda_graph(D, causal):
+@pytest.mark.parametrize("D,causal,B,H,N", [(64, False, 1, 4, 384), (128, True, 1, 4, 384),
+                                           (64, False, 1, 16, 8192)])  # pairs, then a dependent single-tile launch
+def test_forward_replays_from_a_cuda_graph(D, causal, B, H, N):
     torch = torch_cuda()
     import attention_forward_12_gb300 as attn
     attn.build()
-    B, H, N = 1, 4, 384
+    if N == 8192:
+        assert attn.fwd_launch_count(B, H, N, N, D, causal) == 2
     bufs = [torch.from_numpy(x).cuda() for x in synth.make_qkv(B, H, N, N, D, seed=31)]
     o = torch.empty_like(bufs[0])
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
