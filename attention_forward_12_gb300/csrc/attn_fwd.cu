@@ -276,6 +276,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // many CTAs doing half the work each: the pairs' launch skips them
   // (n_main: the pairs it keeps, in (head, pair) order), and the single-
   // tile launch's CTA b takes query tile b % 2 of pair n_main + b / 2.
+  // Small grids, grids of half-empty pairs and causal grids of at most one
+  // wave of pairs run as single-tile CTAs alone (n_main = 0).
   constexpr bool single = SINGLE;
   static_assert(!SINGLE || (SLOTS == 2 && !SPLITKV), "single-tile CTAs");
   int bh, pair, half = 0;
