@@ -81,7 +81,12 @@ enum {
  *
  * Enqueues one kernel on `stream`, or two for the non-causal forward when
  * the last wave of CTAs would occupy at most half the SMs
- * (attn_fwd_launch_count tells which).
+ * (attn_fwd_launch_count tells which); the second is a programmatic
+ * dependent launch of the first, and the call as a whole completes in
+ * stream order.  The kernels allow programmatic dependents to start early:
+ * a kernel the caller launches next with programmatic stream serialization
+ * must wait on its grid dependency (cudaGridDependencySynchronize) before it
+ * reads O or LSE, as that feature requires anyway.
  *
  * Key range: the keys one row accumulates -- Nk, or min(Nk, Nq) when causal
  * -- must not exceed ATTN_MAX_KEYS_PER_PASS (2^19), else ATTN_ETOOLONG is
