@@ -993,6 +993,9 @@ attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restric
   const size_t row = static_cast<size_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  // Launched as a programmatic dependent of the split forward: wait for
+  // that grid to complete and its parts to be visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // Like the forward, no work while the status word holds an error: the
   // parts of a forward that stopped early were never written.
   if (*static_cast<volatile int*>(&g_attn_status) != 0) return;
@@ -1482,9 +1485,21 @@ int launch_merge(const float* ws_o, const float* ws_l, void* o, float* lse, size
                  cudaStream_t st) {
   const size_t blocks = (rows + 3) / 4;
   if (blocks > 0x7fffffffu) return ATTN_EUNSUPPORTED;
-  attn_splitkv_merge_kernel<HD><<<static_cast<unsigned>(blocks), 128, 0, st>>>(
-      ws_o, ws_l, static_cast<__half*>(o), lse, rows, splits);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
+  // A programmatic dependent launch: the merge's CTAs are placed while the
+  // split forward's last CTAs still run, and wait for its grid in the kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_splitkv_merge_kernel<HD>, ws_o, ws_l,
+                                           static_cast<__half*>(o), lse, rows, splits);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ECUDA;
 }
 
 // The split-KV forward and its merge on `workspace` (parts, then the
